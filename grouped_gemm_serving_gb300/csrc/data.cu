@@ -1,0 +1,200 @@
+// Data movement around the grouped GEMMs (section 1 of "LlamaFactory Triton
+// fused MoE kernel": moe_scatter before the first grouped GEMM, silu(gate) *
+// up between them, moe_gather after the second), all HBM-bound: every
+// kernel moves 16-byte vectors with coalesced loads and stores.
+#include <climits>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerBlock = kThreads / 32;
+
+// Reads L = offsets[E] and checks 0 <= L <= M_cap; a bad value is reported
+// and the caller skips all work.
+__device__ __forceinline__ int live_rows(const int32_t* offsets, int E, int M_cap, int* err) {
+    const int L = offsets[E];
+    if (L < 0 || L > M_cap) {
+        moe::raise_device_error(err, MOE_DEVERR_OFFSETS);
+        return -1;
+    }
+    return L;
+}
+
+// xp[p] = x[sorted_rows[p] / k] for p < L; one warp per row, persistent over rows.
+// row_vecs = bytes per row / 16.  FP8 rows also move their group scales into
+// the group-major layout xp_scales[g * M_cap + p].
+__global__ void __launch_bounds__(kThreads)
+permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, int T, int k,
+               int row_vecs, int G, const int32_t* __restrict__ sorted_rows,
+               const int32_t* __restrict__ offsets, int E, int M_cap, uint4* __restrict__ xp,
+               float* __restrict__ xp_scales, int* err) {
+    const int L = live_rows(offsets, E, M_cap, err);
+    if (L < 0) return;
+    const int lane = threadIdx.x & 31;
+    const int warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int nwarps = gridDim.x * kWarpsPerBlock;
+    for (int p = warp0; p < L; p += nwarps) {
+        const int slot = sorted_rows[p];
+        const int t = slot / k;
+        if (slot < 0 || t >= T) {
+            moe::raise_device_error(err, MOE_DEVERR_ROUTE);
+            continue;
+        }
+        const uint4* src = x + static_cast<int64_t>(t) * row_vecs;
+        uint4* dst = xp + static_cast<int64_t>(p) * row_vecs;
+#pragma unroll 4
+        for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+        if (x_scales)
+            for (int g = lane; g < G; g += 32)
+                xp_scales[static_cast<int64_t>(g) * M_cap + p] = __ldg(x_scales + static_cast<int64_t>(t) * G + g);
+    }
+}
+
+// h = silu(g) * u over 8 columns per thread; rows >= L are zero.
+__global__ void __launch_bounds__(kThreads)
+swiglu_kernel(const uint4* __restrict__ Y1, const int32_t* __restrict__ offsets, int E, int M_cap,
+              int I, uint4* __restrict__ h, int* err) {
+    const int L = live_rows(offsets, E, M_cap, err);
+    if (L < 0) return;
+    const int cv = I / 8;                       // 16-byte vectors per h row
+    const int64_t n = static_cast<int64_t>(M_cap) * cv;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int64_t p = i / cv;
+        const int c = static_cast<int>(i - p * cv);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (p < L) {
+            const uint4 g = __ldg(Y1 + p * 2 * cv + c);
+            const uint4 u = __ldg(Y1 + p * 2 * cv + cv + c);
+            const uint32_t gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w};
+            uint32_t os[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float g0 = moe::bf16_lo(gs[j]), g1 = moe::bf16_hi(gs[j]);
+                const float h0 = g0 / (1.0f + expf(-g0)) * moe::bf16_lo(us[j]);
+                const float h1 = g1 / (1.0f + expf(-g1)) * moe::bf16_hi(us[j]);
+                os[j] = moe::pack_bf16x2(h0, h1);
+            }
+            o = make_uint4(os[0], os[1], os[2], os[3]);
+        }
+        h[i] = o;
+    }
+}
+
+// out[t] = sum_j w[t,j] * Y2[row_pos[t*k+j]] over non-sentinel slots, fp32 in
+// j order; one warp per token, 8 columns (one 16-byte vector) per lane step.
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
+               const float* __restrict__ w, const int32_t* __restrict__ row_pos, int T, int k,
+               int row_vecs, int E, int64_t M_cap, uint4* __restrict__ out, int* err) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (t >= T) return;
+    // lane j < k holds slot j's row (or -1) and weight
+    int my_row = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        const int64_t f = static_cast<int64_t>(t) * k + lane;
+        const int id = ids[f];
+        if (id != E) {
+            const int pos = row_pos[f];
+            if (pos < 0 || pos >= M_cap) {
+                moe::raise_device_error(err, MOE_DEVERR_ROUTE);
+            } else {
+                my_row = pos;
+                my_w = w[f];
+            }
+        }
+    }
+    uint4* dst = out + static_cast<int64_t>(t) * row_vecs;
+    // the trip count is the same for every lane, so the shuffles see a full warp
+    for (int c0 = 0; c0 < row_vecs; c0 += 32) {
+        const int c = c0 + lane;
+        const bool in_row = c < row_vecs;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int row = __shfl_sync(0xffffffffu, my_row, j);
+            const float wj = __shfl_sync(0xffffffffu, my_w, j);
+            if (row < 0 || !in_row) continue;
+            const uint4 v = __ldg(Y2 + static_cast<int64_t>(row) * row_vecs + c);
+            const uint32_t vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj, moe::bf16_lo(vs[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj, moe::bf16_hi(vs[i]), acc[2 * i + 1]);
+            }
+        }
+        if (in_row)
+            dst[c] = make_uint4(moe::pack_bf16x2(acc[0], acc[1]), moe::pack_bf16x2(acc[2], acc[3]),
+                                moe::pack_bf16x2(acc[4], acc[5]), moe::pack_bf16x2(acc[6], acc[7]));
+    }
+}
+
+int persistent_blocks(int64_t work_warps) {
+    const int64_t want = (work_warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t cap = static_cast<int64_t>(moe::sm_count() > 0 ? moe::sm_count() : 148) * 8;
+    return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_permute(moe_dtype_t dtype, const void* x, const float* x_scales, int T,
+                                    int H, int k, const int32_t* sorted_rows,
+                                    const int32_t* offsets, int E, int M_cap, void* xp,
+                                    float* xp_scales, moe_stream_t stream) {
+    MOE_CHECK_ARG(x && sorted_rows && offsets && xp && T >= 1 && H >= 1 && k >= 1 && E >= 1);
+    MOE_CHECK_ARG(static_cast<int64_t>(T) * k <= M_cap && M_cap < INT_MAX);
+    MOE_CHECK_ARG(moe::aligned16(x) && moe::aligned16(xp));
+    const bool fp8 = dtype == MOE_FP8_E4M3_B128;
+    if (!fp8 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    int row_vecs, G = 0;
+    if (fp8) {
+        MOE_CHECK_ARG(H % 128 == 0 && x_scales && xp_scales);
+        row_vecs = H / 16;
+        G = H / 128;
+    } else {
+        MOE_CHECK_ARG(H % 8 == 0);
+        row_vecs = H / 8;
+    }
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+    permute_kernel<<<persistent_blocks(M_cap), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(x), fp8 ? x_scales : nullptr, T, k, row_vecs, G, sorted_rows,
+        offsets, E, M_cap, static_cast<uint4*>(xp), fp8 ? xp_scales : nullptr, err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_swiglu(const void* Y1, const int32_t* offsets, int E, int M_cap, int I,
+                                   void* h, moe_stream_t stream) {
+    MOE_CHECK_ARG(Y1 && offsets && h && E >= 1 && M_cap >= 1 && I >= 8 && I % 8 == 0);
+    MOE_CHECK_ARG(moe::aligned16(Y1) && moe::aligned16(h));
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+    const int64_t vecs = static_cast<int64_t>(M_cap) * (I / 8);
+    const int blocks = persistent_blocks((vecs + 31) / 32);
+    swiglu_kernel<<<blocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(Y1), offsets, E, M_cap, I, static_cast<uint4*>(h), err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* topk_w,
+                                    const int32_t* row_pos, int T, int k, int H, int E, void* out,
+                                    moe_stream_t stream) {
+    MOE_CHECK_ARG(Y2 && topk_ids && topk_w && row_pos && out);
+    MOE_CHECK_ARG(T >= 1 && k >= 1 && k <= 32 && E >= 1 && H >= 8 && H % 8 == 0);
+    MOE_CHECK_ARG(moe::aligned16(Y2) && moe::aligned16(out));
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+    const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    combine_kernel<<<blocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(Y2), topk_ids, topk_w, row_pos, T, k, H / 8, E,
+        static_cast<int64_t>(T) * k, static_cast<uint4*>(out), err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}

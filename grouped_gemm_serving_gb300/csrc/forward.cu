@@ -1,0 +1,155 @@
+// moe_forward: the whole expert layer enqueued on one stream, in the order of
+// the fused pipeline of "LlamaFactory Triton fused MoE kernel" (section 1):
+// route + sort -> [quantise x] -> scatter -> grouped GEMM gate_up with fused
+// silu(gate) * up [and fused FP8 quantisation of h] -> grouped GEMM down ->
+// weighted gather.  Offsets stay on the device; there is no host
+// synchronisation.
+#include "common.cuh"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Carver {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off += (bytes + kAlign - 1) & ~(kAlign - 1);
+        return o;
+    }
+};
+
+struct Layout {
+    size_t route, ids, w, sorted_rows, row_pos, offsets;
+    size_t xq, xs;          // FP8: quantised x and its scales
+    size_t xp, xps;         // permuted activations (+ FP8 scales, group-major)
+    size_t h, hs;           // gate_up output after SwiGLU (+ FP8 scales)
+    size_t y2;              // down output, bf16
+    size_t x_dev, logits_dev, out_dev;  // host-I/O staging
+    size_t total;
+};
+
+bool valid_args(const moe_forward_args* a) {
+    if (!a) return false;
+    if (a->T < 1 || a->E < 1 || a->E > 256 || a->k < 1 || a->k > a->E || a->k > 32) return false;
+    if (a->H < 8 || a->H % 8 || a->I < 8 || a->I % 8) return false;
+    if (static_cast<int64_t>(a->T) * a->k >= (1ll << 31) - 1) return false;
+    if (a->dtype == MOE_FP8_E4M3_B128) {
+        if (a->H % 128 || a->I % 128 || !a->W1_scales || !a->W2_scales) return false;
+    } else if (a->dtype != MOE_BF16) {
+        return false;
+    }
+    if (!a->x || !a->W1 || !a->W2 || !a->out) return false;
+    if (!a->logits && (!a->topk_ids || !a->topk_w)) return false;
+    return true;
+}
+
+Layout layout(const moe_forward_args* a) {
+    const size_t T = a->T, E = a->E, k = a->k, H = a->H, I = a->I, R = T * k;
+    const bool fp8 = a->dtype == MOE_FP8_E4M3_B128;
+    Carver c;
+    Layout l{};
+    l.route = c.take(moe_route_sort_workspace_size(a->T, a->E, a->k));
+    l.ids = a->topk_ids ? 0 : c.take(R * 4);
+    l.w = a->topk_w ? 0 : c.take(R * 4);
+    l.sorted_rows = c.take(R * 4);
+    l.row_pos = c.take(R * 4);
+    l.offsets = c.take((E + 1) * 4);
+    if (fp8) {
+        l.xq = c.take(T * H);
+        l.xs = c.take(T * (H / 128) * 4);
+        l.xp = c.take(R * H);
+        l.xps = c.take((H / 128) * R * 4);
+        l.h = c.take(R * I);
+        l.hs = c.take((I / 128) * R * 4);
+    } else {
+        l.xp = c.take(R * H * 2);
+        l.h = c.take(R * I * 2);
+    }
+    l.y2 = c.take(R * H * 2);
+    if (a->flags & MOE_FWD_HOST_IO) {
+        l.x_dev = c.take(T * H * 2);
+        l.logits_dev = a->logits ? c.take(T * E * 4) : 0;
+        l.out_dev = c.take(T * H * 2);
+    }
+    l.total = c.off;
+    return l;
+}
+
+#define MOE_TRY(call)                          \
+    do {                                       \
+        const moe_status_t st_ = (call);       \
+        if (st_ != MOE_OK) return st_;         \
+    } while (0)
+
+}  // namespace
+
+extern "C" size_t moe_forward_workspace_size(const moe_forward_args* args) {
+    if (!valid_args(args)) return 0;
+    return layout(args).total;
+}
+
+extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
+    if (!valid_args(a)) return MOE_ERR_INVALID_ARG;
+    const Layout l = layout(a);
+    if (!ws || ws_bytes < l.total) return MOE_ERR_WORKSPACE;
+    MOE_CHECK_ARG(moe::aligned16(ws));
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int T = a->T, E = a->E, k = a->k, H = a->H, I = a->I, R = T * k;
+    const bool fp8 = a->dtype == MOE_FP8_E4M3_B128;
+    const bool host_io = (a->flags & MOE_FWD_HOST_IO) != 0;
+
+    const void* x = a->x;
+    const float* logits = a->logits;
+    void* out = a->out;
+    if (host_io) {
+        void* xd = base + l.x_dev;
+        MOE_CHECK_CUDA(cudaMemcpyAsync(xd, a->x, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice, s));
+        x = xd;
+        if (logits) {
+            float* ld = reinterpret_cast<float*>(base + l.logits_dev);
+            MOE_CHECK_CUDA(cudaMemcpyAsync(ld, a->logits, static_cast<size_t>(T) * E * 4,
+                                           cudaMemcpyHostToDevice, s));
+            logits = ld;
+        }
+        out = base + l.out_dev;
+    }
+    int32_t* ids = a->topk_ids ? a->topk_ids : reinterpret_cast<int32_t*>(base + l.ids);
+    float* w = a->topk_w ? a->topk_w : reinterpret_cast<float*>(base + l.w);
+    int32_t* sorted_rows = reinterpret_cast<int32_t*>(base + l.sorted_rows);
+    int32_t* row_pos = reinterpret_cast<int32_t*>(base + l.row_pos);
+    int32_t* offsets = reinterpret_cast<int32_t*>(base + l.offsets);
+
+    MOE_TRY(moe_route_sort(logits, a->expert_bias, a->sentinel_mask, ids, w, T, E, k, a->renormalize,
+                           sorted_rows, row_pos, offsets, base + l.route,
+                           moe_route_sort_workspace_size(T, E, k), stream));
+    void* y2 = base + l.y2;
+    if (!fp8) {
+        void* xp = base + l.xp;
+        void* h = base + l.h;
+        MOE_TRY(moe_permute(MOE_BF16, x, nullptr, T, H, k, sorted_rows, offsets, E, R, xp, nullptr, stream));
+        MOE_TRY(moe_grouped_gemm(MOE_BF16, xp, nullptr, a->W1, nullptr, offsets, E, R, 2 * I, H,
+                                 MOE_EPI_SWIGLU, h, nullptr, stream));
+        MOE_TRY(moe_grouped_gemm(MOE_BF16, h, nullptr, a->W2, nullptr, offsets, E, R, H, I,
+                                 MOE_EPI_STORE, y2, nullptr, stream));
+    } else {
+        uint8_t* xq = base + l.xq;
+        float* xs = reinterpret_cast<float*>(base + l.xs);
+        uint8_t* xp = base + l.xp;
+        float* xps = reinterpret_cast<float*>(base + l.xps);
+        uint8_t* h = base + l.h;
+        float* hs = reinterpret_cast<float*>(base + l.hs);
+        MOE_TRY(moe_act_quant_fp8(x, T, H, xq, xs, stream));
+        MOE_TRY(moe_permute(MOE_FP8_E4M3_B128, xq, xs, T, H, k, sorted_rows, offsets, E, R, xp, xps, stream));
+        MOE_TRY(moe_grouped_gemm(MOE_FP8_E4M3_B128, xp, xps, a->W1, a->W1_scales, offsets, E, R, 2 * I, H,
+                                 MOE_EPI_SWIGLU_QUANT_FP8, h, hs, stream));
+        MOE_TRY(moe_grouped_gemm(MOE_FP8_E4M3_B128, h, hs, a->W2, a->W2_scales, offsets, E, R, H, I,
+                                 MOE_EPI_STORE, y2, nullptr, stream));
+    }
+    MOE_TRY(moe_combine(y2, ids, w, row_pos, T, k, H, E, out, stream));
+    if (host_io)
+        MOE_CHECK_CUDA(cudaMemcpyAsync(a->out, out, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}

@@ -1,0 +1,601 @@
+// moe_grouped_gemm: the per-expert GEMMs of the MoE layer on the
+// fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
+// operands staged by TMA.
+//
+// Sources: group_gemm_same_nk for fc1 and fc2 with silu(gate) * up between
+// them (section 1 of "LlamaFactory Triton fused MoE kernel");
+// grouped_fp8_matmul with 128x128-block weight scales and per-token,
+// per-128-column activation scales (section 1 of "Hugging Face Transformers:
+// MoE and FP8 kernel optimisation"); sentinel rows neither computed nor left
+// uninitialised (sections 2 and 3 of the same write-up); one grouped GEMM
+// over rows sorted by expert id (grouped_mm backend, "Mixture of Experts in
+// transformers").
+//
+// Design (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile [128 rows x 128 bytes] and B tile
+//               [256 rows x 128 bytes] per k-block into a 4-stage ring;
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32 bytes) per
+//               k-block into one of two 256-column TMEM accumulators;
+//   warps 2-9   epilogue: tcgen05.ld the accumulator, apply the epilogue and
+//               store; warp w reads TMEM lanes 32*(w%4).., columns half
+//               (w-2)/4; then zero the sentinel rows [offsets[E], M_cap).
+// The tile list is built on the device from offsets: expert e owns
+// ceil(cnt_e/128) row tiles times n_tiles column tiles, ordered expert-major,
+// then column tile, then row tile, so CTAs that run at the same time share a
+// weight tile in L2.  No tile is issued for sentinel rows.
+//
+// bf16: the accumulator sums all k-blocks of a tile in TMEM (double-buffered
+// across tiles).  FP8: each 128-wide k-block is an exact e4m3 x e4m3 partial
+// in TMEM; the epilogue promotes it with sa[row, kb] * sb[block, kb] into fp32
+// registers while the MMA fills the other buffer.
+//
+// Every mbarrier wait is bounded (2 s): on expiry the CTA records
+// MOE_DEVERR_TIMEOUT, stops all roles, waits (bounded) for its in-flight TMA
+// loads and MMAs, frees its tensor memory and exits.
+#include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kStageA = BM * 128;
+constexpr int kStageB = BN * 128;
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kMaxE = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
+
+enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
+
+struct Params {
+    const int32_t* offsets;
+    const float* a_scales;  // FP8: [K/128, M_cap]
+    const float* b_scales;  // FP8: [E, nb_scale, K/128]
+    void* out;              // bf16 [M_cap, out_cols], or e4m3 for EPI_SWIGLU_Q
+    float* out_scales;      // EPI_SWIGLU_Q: [out_cols/128, M_cap]
+    int* err;
+    int E, M_cap, N, K;
+    int half;      // SwiGLU: N/2 (gate rows [0, half), up rows [half, N))
+    int out_cols;  // N (store) or N/2 (SwiGLU)
+    int n_tiles, k_blocks, nb_scale;
+};
+
+struct Shared {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t xbar[2];  // amax exchange of the quantising epilogue
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int valid;
+    int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
+    float amax_x[2][2][BM];
+};
+
+constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Shared);
+
+struct Tile {
+    int e, row0, row_end, col0;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params& p) {
+    int lo = 0, hi = p.E;  // largest e < E with prefix[e] * n_tiles <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (S.prefix[mid] * p.n_tiles <= t) lo = mid; else hi = mid;
+    }
+    const int mt = S.prefix[lo + 1] - S.prefix[lo];
+    const int local = t - S.prefix[lo] * p.n_tiles;
+    Tile ti;
+    ti.e = lo;
+    ti.row0 = p.offsets[lo] + (local % mt) * BM;
+    ti.row_end = p.offsets[lo + 1];
+    ti.col0 = (local / mt) * (p.half ? BN / 2 : BN);
+    return ti;
+}
+
+__device__ __forceinline__ void fail(Shared& S, const Params& p) {
+    S.abort_flag = 1;
+    moe::raise_device_error(p.err, MOE_DEVERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t bar(uint64_t& b) { return moe::smem_u32(&b); }
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// 32 consecutive fp32 values -> bf16, stored as four 16-byte vectors whose
+// columns lie below ncols (ncols is a multiple of 8).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* row, int col, int ncols, const float* v) {
+    uint4* dst = reinterpret_cast<uint4*>(row + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (col + 8 * i < ncols)
+            dst[i] = make_uint4(moe::pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                moe::pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                moe::pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                moe::pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float s) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(c, s), __fdiv_rn(d, s)), __NV_SATFINITE, __NV_E4M3);
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// ---------------------------------------------------------------- roles
+template <bool FP8, int EPI>
+__device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* stages,
+                         Shared& S, const Params& p, int total) {
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const Tile ti = decode_tile(t, S, p);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = bar(S.full[stage]);
+            moe::mbar_arrive_expect_tx(fb, kStageBytes);
+            const uint32_t sa = moe::smem_u32(stages + stage * kStageBytes);
+            const uint32_t sb = sa + kStageA;
+            const int kc = kb * (FP8 ? 128 : 64);
+            moe::tma_load_2d(sa, tmA, fb, kc, ti.row0);
+            if (EPI == EPI_STORE) {
+                moe::tma_load_3d(sb, tmB, fb, kc, ti.col0, ti.e);
+            } else {
+                moe::tma_load_4d(sb, tmB, fb, kc, ti.col0, 0, ti.e);
+                moe::tma_load_4d(sb + (BN / 2) * 128, tmB, fb, kc, ti.col0, 1, ti.e);
+            }
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+    }
+    if (!ok) {
+        fail(S, p);
+        int zero = 0;
+        for (int s = 0; s < kStages; ++s)
+            if ((issued >> s) & 1u)
+                moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
+    }
+}
+
+template <bool FP8>
+__device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int total, uint32_t tmem) {
+    constexpr uint32_t idesc = moe::make_idesc(FP8 ? 0u : 1u, BM, BN);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued = false;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        if (!FP8) {
+            if (!moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs)) { ok = false; break; }
+            moe::tc_fence_after();
+        }
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (FP8) {
+                if (!moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs)) { ok = false; break; }
+                moe::tc_fence_after();
+            }
+            if (!moe::mbar_wait(bar(S.full[stage]), phase, &S.abort_flag, kWaitNs)) { ok = false; break; }
+            moe::tc_fence_after();
+            const uint32_t sa = moe::smem_u32(stages + stage * kStageBytes);
+            const uint64_t adesc = moe::smem_desc_sw128(sa);
+            const uint64_t bdesc = moe::smem_desc_sw128(sa + kStageA);
+            const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // 32 bytes of K per instruction; +2 = +32 B start address
+                if (FP8)
+                    moe::mma_fp8(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0);
+                else
+                    moe::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+            moe::tc_commit(bar(S.empty[stage]));
+            issued = true;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            if (FP8) {
+                moe::tc_commit(bar(S.acc_full[acc]));
+                acc ^= 1;
+                if (!acc) acc_phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        if (!FP8) {
+            moe::tc_commit(bar(S.acc_full[acc]));
+            acc ^= 1;
+            if (!acc) acc_phase ^= 1u;
+        }
+    }
+    if (!ok) fail(S, p);
+    if (issued) {  // every MMA of this CTA has finished before TMEM is freed
+        int zero = 0;
+        moe::tc_commit(bar(S.mma_done));
+        moe::mbar_wait(bar(S.mma_done), 0, &zero, kDrainNs);
+    }
+}
+
+template <bool FP8, int EPI>
+__device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int hsel = (warp - 2) >> 2;     // which half of the tile's columns
+    const int r = q * 32 + lane;          // accumulator row of this thread
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    int acc = 0, xsel = 0;
+    uint32_t acc_phase = 0, xphase = 0;
+    const int KB = p.k_blocks;
+
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const Tile ti = decode_tile(t, S, p);
+        const int row = ti.row0 + r;
+        const bool live = row < ti.row_end;
+        if (!FP8) {
+            if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
+            moe::tc_fence_after();
+            const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.out_cols;
+            if (EPI == EPI_STORE) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
+                    moe::tmem_ld_wait();
+                    if (live) store_bf16x32(orow, ti.col0 + hsel * 128 + c * 32, p.out_cols,
+                                            reinterpret_cast<const float*>(v));
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t g[32], u[32];
+                    moe::tmem_ld32(ta + hsel * 64 + c * 32, g);
+                    moe::tmem_ld32(ta + 128 + hsel * 64 + c * 32, u);
+                    moe::tmem_ld_wait();
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) h[i] = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                    if (live) store_bf16x32(orow, ti.col0 + hsel * 64 + c * 32, p.out_cols, h);
+                }
+            }
+            moe::tc_fence_before();
+            moe::mbar_arrive(bar(S.acc_empty[acc]));
+            acc ^= 1;
+            if (!acc) acc_phase ^= 1u;
+        } else {
+            float a[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) a[i] = 0.0f;
+            const float* sb_row = p.b_scales + static_cast<int64_t>(ti.e) * p.nb_scale * KB;
+            const int nb0 = EPI == EPI_STORE ? (ti.col0 + hsel * 128) / 128 : ti.col0 / 128;
+            const int nb1 = EPI == EPI_STORE ? nb0 : (p.half + ti.col0) / 128;
+            const bool nb_ok = nb0 < p.nb_scale;
+            for (int kb = 0; kb < KB; ++kb) {
+                const float sa = row < p.M_cap ? __ldg(p.a_scales + static_cast<int64_t>(kb) * p.M_cap + row) : 0.0f;
+                const float s0 = nb_ok ? sa * __ldg(sb_row + nb0 * KB + kb) : 0.0f;
+                const float s1 = EPI == EPI_STORE ? s0 : sa * __ldg(sb_row + nb1 * KB + kb);
+                if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
+                moe::tc_fence_after();
+                const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
+                if (EPI == EPI_STORE) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
+                        moe::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[c * 32 + i] = fmaf(s0, __uint_as_float(v[i]), a[c * 32 + i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t g[32], u[32];
+                        moe::tmem_ld32(ta + hsel * 64 + c * 32, g);
+                        moe::tmem_ld32(ta + 128 + hsel * 64 + c * 32, u);
+                        moe::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            a[c * 32 + i] = fmaf(s0, __uint_as_float(g[i]), a[c * 32 + i]);
+                            a[64 + c * 32 + i] = fmaf(s1, __uint_as_float(u[i]), a[64 + c * 32 + i]);
+                        }
+                    }
+                }
+                moe::tc_fence_before();
+                moe::mbar_arrive(bar(S.acc_empty[acc]));
+                acc ^= 1;
+                if (!acc) acc_phase ^= 1u;
+            }
+            if (EPI == EPI_STORE) {
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.out_cols;
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) store_bf16x32(orow, ti.col0 + hsel * 128 + c * 32, p.out_cols, a + c * 32);
+                }
+            } else if (EPI == EPI_SWIGLU) {
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.out_cols;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) a[i] = silu_mul(a[i], a[64 + i]);
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) store_bf16x32(orow, ti.col0 + hsel * 64 + c * 32, p.out_cols, a + c * 32);
+                }
+            } else {
+                // h rounded to bf16, then quantised per 128 columns; the two
+                // threads holding a row's halves exchange their amax.
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    a[i] = __bfloat162float(__float2bfloat16_rn(silu_mul(a[i], a[64 + i])));
+                    amax = fmaxf(amax, fabsf(a[i]));
+                }
+                S.amax_x[xsel][hsel][r] = amax;
+                moe::mbar_arrive(bar(S.xbar[xsel]));
+                if (!moe::mbar_wait(bar(S.xbar[xsel]), xphase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
+                amax = fmaxf(amax, S.amax_x[xsel][hsel ^ 1][r]);
+                xsel ^= 1;
+                if (!xsel) xphase ^= 1u;
+                const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+                if (live) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                                          static_cast<int64_t>(row) * p.out_cols +
+                                                          ti.col0 + hsel * 64);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const float* h = a + 16 * v;
+                        dst[v] = make_uint4(quant4(h[0], h[1], h[2], h[3], s), quant4(h[4], h[5], h[6], h[7], s),
+                                            quant4(h[8], h[9], h[10], h[11], s),
+                                            quant4(h[12], h[13], h[14], h[15], s));
+                    }
+                    if (hsel == 0) p.out_scales[static_cast<int64_t>(ti.col0 / 128) * p.M_cap + row] = s;
+                }
+            }
+        }
+    }
+}
+
+// Sentinel rows [offsets[E], M_cap) of the output: zeros (q = 0 and scale 1
+// for the quantising epilogue), spread over every epilogue thread of the grid.
+template <int EPI>
+__device__ void zero_sentinel_rows(const Params& p) {
+    const int L = p.offsets[p.E];
+    const int64_t rows = static_cast<int64_t>(p.M_cap) - L;
+    if (rows <= 0) return;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kEpiThreads + (threadIdx.x - 64);
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * kEpiThreads;
+    const int esz = EPI == EPI_SWIGLU_Q ? 1 : 2;
+    const int64_t vpr = static_cast<int64_t>(p.out_cols) * esz / 16;
+    uint4* base = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + static_cast<int64_t>(L) * p.out_cols * esz);
+    for (int64_t i = tid; i < rows * vpr; i += nthr) base[i] = make_uint4(0, 0, 0, 0);
+    if (EPI == EPI_SWIGLU_Q) {
+        const int G = p.out_cols / 128;
+        for (int64_t i = tid; i < rows * G; i += nthr) {
+            const int64_t g = i / rows, rr = i - g * rows;
+            p.out_scales[g * p.M_cap + L + rr] = 1.0f;
+        }
+    }
+}
+
+template <bool FP8, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared& S = *reinterpret_cast<Shared*>(stages + kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            moe::mbar_init(bar(S.full[s]), 1);
+            moe::mbar_init(bar(S.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            moe::mbar_init(bar(S.acc_full[a]), 1);
+            moe::mbar_init(bar(S.acc_empty[a]), kEpiThreads);
+            moe::mbar_init(bar(S.xbar[a]), kEpiThreads);
+        }
+        moe::mbar_init(bar(S.mma_done), 1);
+        S.abort_flag = 0;
+        moe::fence_barrier_init();
+    }
+    if (warp == 0) {
+        // validate offsets and build the row-tile prefix (8 experts per lane)
+        int mt[8], sum = 0, bad = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            mt[i] = 0;
+            if (e < p.E) {
+                const int lo = p.offsets[e], hi = p.offsets[e + 1];
+                if (hi < lo) bad = 1;
+                mt[i] = hi > lo ? (hi - lo + BM - 1) / BM : 0;
+                sum += mt[i];
+            }
+        }
+        if (lane == 0 && (p.offsets[0] != 0 || p.offsets[p.E] > p.M_cap)) bad = 1;
+        bad = __any_sync(0xffffffffu, bad);
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < p.E) { S.prefix[e] = run; run += mt[i]; }
+        }
+        if (lane == 31) S.prefix[p.E] = incl;
+        if (lane == 0) {
+            S.valid = !bad;
+            if (bad && blockIdx.x == 0) moe::raise_device_error(p.err, MOE_DEVERR_OFFSETS);
+        }
+    } else if (warp == 1 && lane == 0) {
+        moe::prefetch_tensormap(&tmA);
+        moe::prefetch_tensormap(&tmB);
+    }
+    __syncthreads();
+    if (!S.valid) return;
+    if (warp == 1) {
+        moe::tmem_alloc(moe::smem_u32(&S.tmem_base), kTmemCols);
+        moe::tmem_relinquish();
+    }
+    moe::tc_fence_before();
+    __syncthreads();
+    moe::tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+    const int total = S.prefix[p.E] * p.n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer<FP8>(stages, S, p, total, tmem);
+        __syncwarp();
+    } else {
+        epilogue<FP8, EPI>(S, p, total, tmem);
+        zero_sentinel_rows<EPI>(p);
+    }
+    moe::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        moe::tc_fence_after();
+        moe::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap* map, bool fp8, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FP8, int EPI>
+moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p, cudaStream_t s) {
+    auto kern = grouped_gemm_kernel<FP8, EPI>;
+    static int configured[64] = {0};
+    int dev = 0;
+    MOE_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (!configured[dev]) {
+        MOE_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemBytes)));
+        configured[dev] = 1;
+    }
+    const int grid = moe::sm_count();
+    if (grid <= 0) return MOE_ERR_CUDA;
+    kern<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,
+                                         const void* B, const float* B_scales, const int32_t* offsets,
+                                         int E, int M_cap, int N, int K, moe_epilogue_t epilogue,
+                                         void* C, float* C_scales, moe_stream_t stream) {
+    MOE_CHECK_ARG(A && B && offsets && C && E >= 1 && E <= kMaxE && M_cap >= 1 && N >= 8 && K >= 8);
+    MOE_CHECK_ARG(moe::aligned16(A) && moe::aligned16(B) && moe::aligned16(C));
+    const bool fp8 = dtype == MOE_FP8_E4M3_B128;
+    if (!fp8 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    const bool swiglu = epilogue == MOE_EPI_SWIGLU || epilogue == MOE_EPI_SWIGLU_QUANT_FP8;
+    if (epilogue != MOE_EPI_STORE && !swiglu) return MOE_ERR_INVALID_ARG;
+    if (epilogue == MOE_EPI_SWIGLU_QUANT_FP8 && !fp8) return MOE_ERR_UNSUPPORTED;
+    if (swiglu) MOE_CHECK_ARG(N % 16 == 0); else MOE_CHECK_ARG(N % 8 == 0);
+    if (fp8) {
+        MOE_CHECK_ARG(K % 128 == 0 && A_scales && B_scales);
+        MOE_CHECK_ARG(moe::aligned16(A_scales) && moe::aligned16(B_scales));
+        if (swiglu) MOE_CHECK_ARG((N / 2) % 128 == 0);
+        if (epilogue == MOE_EPI_SWIGLU_QUANT_FP8) MOE_CHECK_ARG(C_scales && moe::aligned16(C_scales));
+    } else {
+        MOE_CHECK_ARG(K % 8 == 0);
+    }
+    const int half = swiglu ? N / 2 : 0;
+    const int n_tiles = swiglu ? (half + BN / 2 - 1) / (BN / 2) : (N + BN - 1) / BN;
+    const int64_t max_tiles = (static_cast<int64_t>(M_cap) / BM + E) * n_tiles;
+    MOE_CHECK_ARG(max_tiles < INT_MAX);
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+
+    const int esz = fp8 ? 1 : 2;
+    const cuuint32_t bk = 128 / esz;  // elements in a 128-byte k-block row
+    CUtensorMap tmA, tmB;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M_cap)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * esz};
+        const cuuint32_t box[2] = {bk, BM};
+        if (!encode(&tmA, fp8, A, 2, dims, strides, box)) return MOE_ERR_CUDA;
+    }
+    if (!swiglu) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(N) * K * esz};
+        const cuuint32_t box[3] = {bk, BN, 1};
+        if (!encode(&tmB, fp8, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
+    } else {
+        // [E, 2, N/2, K]: a gate box clips at N/2 instead of running into the up rows
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(half), 2,
+                                    static_cast<cuuint64_t>(E)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(half) * K * esz,
+                                       static_cast<cuuint64_t>(N) * K * esz};
+        const cuuint32_t box[4] = {bk, BN / 2, 1, 1};
+        if (!encode(&tmB, fp8, B, 4, dims, strides, box)) return MOE_ERR_CUDA;
+    }
+
+    Params p;
+    p.offsets = offsets;
+    p.a_scales = A_scales;
+    p.b_scales = B_scales;
+    p.out = C;
+    p.out_scales = C_scales;
+    p.err = err;
+    p.E = E;
+    p.M_cap = M_cap;
+    p.N = N;
+    p.K = K;
+    p.half = half;
+    p.out_cols = swiglu ? half : N;
+    p.n_tiles = n_tiles;
+    p.k_blocks = (K + static_cast<int>(bk) - 1) / static_cast<int>(bk);
+    p.nb_scale = (N + 127) / 128;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fp8) {
+        if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, p, s);
+        if (epilogue == MOE_EPI_SWIGLU) return launch<true, EPI_SWIGLU>(tmA, tmB, p, s);
+        return launch<true, EPI_SWIGLU_Q>(tmA, tmB, p, s);
+    }
+    if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE>(tmA, tmB, p, s);
+    return launch<false, EPI_SWIGLU>(tmA, tmB, p, s);
+}

@@ -1,0 +1,277 @@
+// moe_route_sort: top-k routing, sentinel marking, per-expert histogram and
+// the stable counting sort of the routed slots by expert id.
+//
+// Routing follows "Mixture of Experts in transformers" (MoE basics: the
+// router picks k of the E experts per token); the sort follows section 2 of
+// "Hugging Face Transformers: MoE and FP8 kernel optimisation": sentinel
+// slots (id E) are left out of the histogram and sort after every live slot,
+// so offsets[E] counts the live rows and no sentinel lands on the last expert.
+//
+// Kernels (one stream, no host synchronisation):
+//   1. route_topk_hist  one warp per token: k rounds of warp arg-max over
+//                       l' = logits + bias (ties to the lower id), softmax
+//                       weights, sentinel mask; then a warp-aggregated
+//                       (__match_any_sync) atomic histogram per sort block.
+//   2. route_scatter    one CTA per sort block of up to 2048 slots: global
+//                       bin starts from the histograms (warp shuffle scan),
+//                       then a stable in-order rank of every slot from
+//                       per-warp match_any peer masks.  Writes sorted_rows,
+//                       row_pos and (block 0) offsets.
+#include <climits>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxSlotsPerBlock = 2048;
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 32;
+
+struct SortGeometry {
+    int tokens_per_block;  // tokens whose slots form one sort block
+    int slots_per_block;
+    int blocks;
+};
+
+SortGeometry geometry(int T, int k) {
+    SortGeometry g;
+    g.tokens_per_block = kMaxSlotsPerBlock / k > 0 ? kMaxSlotsPerBlock / k : 1;
+    g.slots_per_block = g.tokens_per_block * k;
+    g.blocks = (T + g.tokens_per_block - 1) / g.tokens_per_block;
+    return g;
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+// Ids outside [0, E] cannot be placed: they are sorted as sentinels and the
+// error word records the bad input.
+__device__ __forceinline__ int checked_id(int id, int E, int* err) {
+    if (id < 0 || id > E) {
+        moe::raise_device_error(err, MOE_DEVERR_ROUTE);
+        return E;
+    }
+    return id;
+}
+
+__global__ void __launch_bounds__(kThreads)
+route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias,
+                const uint8_t* __restrict__ mask, int32_t* ids, float* __restrict__ w, int T,
+                int E, int k, int renormalize, int slots_per_block, int* counts, int* err) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int64_t slot0 = static_cast<int64_t>(t) * k;
+    int my_id = E;  // lane j < k: the id of slot j
+
+    if (logits) {
+        constexpr int NV = kMaxE / 32;
+        const float* row = logits + static_cast<int64_t>(t) * E;
+        float v[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E) {
+                const float l = row[e];
+                v[j] = bias ? l + bias[e] : l;
+            } else {
+                v[j] = -INFINITY;
+            }
+        }
+        uint32_t taken = 0;
+        float my_v = -INFINITY;
+        for (int r = 0; r < k; ++r) {
+            float bv = -INFINITY;
+            int bi = INT_MAX;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const int e = lane + 32 * j;
+                if (!((taken >> j) & 1u) && better(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == r) { my_v = bv; my_id = bi; }
+        }
+        const float mx = __shfl_sync(0xffffffffu, my_v, 0);  // pick 0 is the maximum
+        float part = 0.0f;
+        if (renormalize) {
+            part = lane < k ? expf(my_v - mx) : 0.0f;
+        } else {
+#pragma unroll
+            for (int j = 0; j < NV; ++j)
+                if (lane + 32 * j < E) part += expf(v[j] - mx);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane < k) {
+            w[slot0 + lane] = expf(my_v - mx) / part;
+            if (mask && mask[slot0 + lane]) my_id = E;
+            ids[slot0 + lane] = my_id;
+        }
+    } else if (lane < k) {
+        my_id = ids[slot0 + lane];
+        if (mask && mask[slot0 + lane]) {
+            my_id = E;
+            ids[slot0 + lane] = E;
+        }
+    }
+    if (lane < k) my_id = checked_id(my_id, E, err);
+
+    // histogram of this token's slots into its sort block, one atomic per
+    // distinct id in the warp
+    const unsigned active = __ballot_sync(0xffffffffu, lane < k);
+    if (lane < k) {
+        const unsigned peers = __match_any_sync(active, my_id);
+        if (lane == __ffs(peers) - 1) {
+            const int blk = static_cast<int>(slot0 / slots_per_block);
+            atomicAdd(&counts[blk * (E + 1) + my_id], __popc(peers));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nblocks,
+              const int* __restrict__ counts, int32_t* __restrict__ sorted_rows,
+              int32_t* __restrict__ row_pos, int32_t* __restrict__ offsets, int* err) {
+    __shared__ int tot[kMaxE + 1];
+    __shared__ int start[kMaxE + 1];
+    __shared__ int whist[kWarps][kMaxE + 1];
+    const int nb = E + 1;
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // 1. per bin: total over all blocks and the count in blocks before this one
+    for (int bin = threadIdx.x; bin < nb; bin += kThreads) {
+        int all = 0, before = 0;
+        for (int bb = 0; bb < nblocks; ++bb) {
+            const int c = counts[bb * nb + bin];
+            all += c;
+            before += bb < b ? c : 0;
+        }
+        tot[bin] = all;
+        start[bin] = before;
+    }
+    for (int i = threadIdx.x; i < kWarps * nb; i += kThreads) whist[i / nb][i % nb] = 0;
+    __syncthreads();
+
+    // 2. exclusive scan of the totals over bins (warp 0: 9 bins per lane)
+    if (warp == 0) {
+        constexpr int PER = (kMaxE + 1 + 31) / 32;
+        int local[PER];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int bin = lane * PER + i;
+            local[i] = bin < nb ? tot[bin] : 0;
+            sum += local[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int bin = lane * PER + i;
+            if (bin < nb) {
+                const int bin_start = run;
+                run += local[i];
+                if (b == 0) offsets[bin] = bin_start;   // offsets[E] = live rows
+                start[bin] += bin_start;                // global base of this block's slots
+            }
+        }
+    }
+    __syncthreads();
+
+    // 3. stable ranks: warp w owns a contiguous run of the block's slots
+    const int64_t blk0 = static_cast<int64_t>(b) * slots_per_block;
+    const int64_t blk1 = blk0 + slots_per_block < R ? blk0 + slots_per_block : R;
+    const int per_warp = (slots_per_block + kWarps - 1) / kWarps;
+    const int64_t w0 = blk0 + static_cast<int64_t>(warp) * per_warp;
+    const int64_t w1 = w0 + per_warp < blk1 ? w0 + per_warp : blk1;
+    const unsigned lt = (1u << lane) - 1u;
+
+    for (int64_t base = w0; base < w1; base += 32) {           // pass A: per-warp histogram
+        const int64_t s = base + lane;
+        const int id = s < w1 ? checked_id(ids[s], E, err) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        if (id >= 0 && lane == __ffs(peers) - 1) whist[warp][id] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int bin = threadIdx.x; bin < nb; bin += kThreads) {   // exclusive prefix over warps
+        int acc = 0;
+        for (int wi = 0; wi < kWarps; ++wi) {
+            const int c = whist[wi][bin];
+            whist[wi][bin] = acc;
+            acc += c;
+        }
+    }
+    __syncthreads();
+    for (int64_t base = w0; base < w1; base += 32) {           // pass B: positions
+        const int64_t s = base + lane;
+        const int id = s < w1 ? checked_id(ids[s], E, err) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        int pos = 0;
+        if (id >= 0) pos = start[id] + whist[warp][id] + __popc(peers & lt);
+        __syncwarp();
+        if (id >= 0) {
+            sorted_rows[pos] = static_cast<int32_t>(s);
+            row_pos[s] = pos;
+            if (lane == __ffs(peers) - 1) whist[warp][id] += __popc(peers);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+extern "C" size_t moe_route_sort_workspace_size(int T, int E, int k) {
+    if (T < 1 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) return 0;
+    const SortGeometry g = geometry(T, k);
+    const size_t bytes = static_cast<size_t>(g.blocks) * (E + 1) * sizeof(int);
+    return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+extern "C" moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
+                                       const uint8_t* sentinel_mask, int32_t* topk_ids,
+                                       float* topk_w, int T, int E, int k, int renormalize,
+                                       int32_t* sorted_rows, int32_t* row_pos, int32_t* offsets,
+                                       void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_CHECK_ARG(T >= 1 && E >= 1 && E <= kMaxE && k >= 1 && k <= E && k <= kMaxK);
+    MOE_CHECK_ARG(static_cast<int64_t>(T) * k < INT_MAX);
+    MOE_CHECK_ARG(topk_ids && sorted_rows && row_pos && offsets);
+    MOE_CHECK_ARG(!logits || topk_w);
+    MOE_CHECK_ARG(moe::aligned16(topk_ids) && moe::aligned16(sorted_rows) &&
+                  moe::aligned16(row_pos) && moe::aligned16(offsets));
+    MOE_CHECK_ARG(!logits || (moe::aligned16(logits) && moe::aligned16(topk_w)));
+    MOE_CHECK_ARG(!expert_bias || moe::aligned16(expert_bias));
+    const size_t need = moe_route_sort_workspace_size(T, E, k);
+    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const SortGeometry g = geometry(T, k);
+    int* counts = static_cast<int*>(ws);
+    MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(g.blocks) * (E + 1) * sizeof(int), s));
+    route_topk_hist<<<(T + kWarps - 1) / kWarps, kThreads, 0, s>>>(
+        logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
+        renormalize, g.slots_per_block, counts, err);
+    MOE_CHECK_LAUNCH();
+    route_scatter<<<g.blocks, kThreads, 0, s>>>(topk_ids, static_cast<int64_t>(T) * k, E,
+                                                g.slots_per_block, g.blocks, counts, sorted_rows,
+                                                row_pos, offsets, err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}

@@ -214,3 +214,32 @@ def sweep_offsets(sw: Sweep) -> np.ndarray:
     if sw.live % sw.E:
         raise ValueError("live rows must split equally over the experts")
     return (np.arange(sw.E + 1, dtype=np.int64) * (sw.live // sw.E)).astype(np.int32)
+
+
+def grouped_offsets(E: int, live: int, seed: int = 0, empty_experts: int = 0) -> np.ndarray:
+    """int32 ``[E+1]`` boundaries of ``live`` rows split at random over E
+    experts (multinomial), with ``empty_experts`` of them forced to zero rows."""
+    g = _rng(seed, _SWEEP_A, 1)
+    p = g.random(E) + 0.05
+    if empty_experts:
+        p[g.choice(E, empty_experts, replace=False)] = 0.0
+    counts = g.multinomial(live, p / p.sum())
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def grouped_rows(M_cap: int, K: int, live: int, seed: int = 0, std: float = 1.0) -> np.ndarray:
+    """bf16 bits ``[M_cap, K]``: N(0, std) for the first ``live`` rows, NaN after."""
+    a = _rng(seed, _SWEEP_A, 2).standard_normal((M_cap, K), dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    a = to_bf16_bits(a)
+    a[live:] = BF16_NAN
+    return a
+
+
+def dense_rows(M: int, K: int, seed: int, std: float = 1.0, tensor_id: int = 3) -> np.ndarray:
+    """bf16 bits ``[M, K]`` N(0, std) -- generic activations for kernel tests."""
+    a = _rng(seed, tensor_id, 17).standard_normal((M, K), dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    return to_bf16_bits(a)

@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every entry point that include/moe.h declares, and rejects bad arguments on
+the host before anything is launched."""
+import os
+import re
+
+import pytest
+
+from grouped_gemm_serving_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    gbuild.build()
+    from grouped_gemm_serving_gb300 import moe as m
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(moe):
+    names = _declared()
+    assert {"moe_route_sort", "moe_permute", "moe_act_quant_fp8", "moe_grouped_gemm", "moe_swiglu",
+            "moe_combine", "moe_forward"} <= set(names)
+    lib = moe.lib()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding wraps every declared entry point under the same name
+    assert all(hasattr(moe, n) or n == "moe_status_string" for n in names)
+
+
+def test_abi_version_and_status_strings(moe):
+    assert moe.moe_abi_version() == 1
+    for st in range(7):
+        assert moe.status_string(st) not in ("", "unknown status")
+
+
+def test_workspace_sizes(moe):
+    assert moe.moe_route_sort_workspace_size(0, 8, 2) == 0
+    assert moe.moe_route_sort_workspace_size(64, 300, 2) == 0
+    assert moe.moe_route_sort_workspace_size(8192, 128, 8) >= 32 * 129 * 4
+    a = moe.forward_args(dtype=moe.MOE_BF16, T=4096, E=32, k=4, H=2880, I=2880, x=1 << 20, W1=1 << 21,
+                         W2=1 << 22, out=1 << 23, logits=1 << 24)
+    R = 4096 * 4
+    assert moe.moe_forward_workspace_size(a) >= R * 2880 * 2 * 2 + R * 2880 * 2
+    bad = moe.forward_args(dtype=moe.MOE_FP8_E4M3_B128, T=64, E=8, k=2, H=2880, I=2880, x=1 << 20,
+                           W1=1 << 21, W2=1 << 22, out=1 << 23, logits=1 << 24)
+    assert moe.moe_forward_workspace_size(bad) == 0   # FP8 needs multiples of 128 and scales
+
+
+@pytest.mark.parametrize("call", [
+    # (function, args) that must fail host-side with MOE_ERR_INVALID_ARG
+    ("moe_route_sort", (None, None, None, None, None, 0, 8, 2, 1, None, None, None, None, 0, None)),
+    ("moe_route_sort", (16, None, None, 16, 16, 4, 300, 2, 1, 16, 16, 16, 16, 1 << 20, None)),
+    ("moe_route_sort", (16, None, None, 16, 16, 4, 8, 9, 1, 16, 16, 16, 16, 1 << 20, None)),
+    ("moe_route_sort", (17, None, None, 16, 16, 4, 8, 2, 1, 16, 16, 16, 16, 1 << 20, None)),
+    ("moe_act_quant_fp8", (16, 4, 100, 16, 16, None)),
+    ("moe_act_quant_fp8", (18, 4, 128, 16, 16, None)),
+    ("moe_weight_quant_fp8", (16, 2, 64, 96, 16, 16, None)),
+    ("moe_permute", (0, 16, None, 4, 12, 2, 16, 16, 8, 8, 16, 16, None)),
+    ("moe_permute", (1, 16, None, 4, 128, 2, 16, 16, 8, 8, 16, 16, None)),
+    ("moe_permute", (0, 16, None, 4, 16, 2, 16, 16, 8, 7, 16, 16, None)),
+    ("moe_grouped_gemm", (0, 16, None, 16, None, 16, 300, 64, 64, 64, 0, 16, None, None)),
+    ("moe_grouped_gemm", (0, 16, None, 16, None, 16, 8, 64, 60, 64, 0, 16, None, None)),
+    ("moe_grouped_gemm", (1, 16, None, 16, None, 16, 8, 64, 256, 128, 0, 16, None, None)),
+    ("moe_grouped_gemm", (1, 16, 16, 16, 16, 16, 8, 64, 256, 100, 0, 16, None, None)),
+    ("moe_grouped_gemm", (1, 16, 16, 16, 16, 16, 8, 64, 192, 128, 1, 16, None, None)),
+    ("moe_grouped_gemm", (0, 16, None, 16, None, 16, 8, 64, 256, 64, 7, 16, None, None)),
+    ("moe_swiglu", (16, 16, 8, 64, 12, 16, None)),
+    ("moe_combine", (16, 16, 16, 16, 4, 2, 12, 8, 16, None)),
+    ("moe_combine", (16, 16, 16, 16, 4, 40, 16, 64, 16, None)),
+])
+def test_host_side_argument_checks(moe, call):
+    name, args = call
+    assert getattr(moe.lib(), name)(*args) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_bf16_quantising_epilogue_is_unsupported(moe):
+    st = moe.lib().moe_grouped_gemm(0, 16, None, 16, None, 16, 8, 64, 256, 64, 2, 16, None, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_workspace_too_small_is_reported(moe):
+    st = moe.lib().moe_route_sort(16, None, None, 16, 16, 64, 8, 2, 1, 16, 16, 16, 16, 4, None)
+    assert st == moe.MOE_ERR_WORKSPACE

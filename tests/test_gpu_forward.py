@@ -1,0 +1,110 @@
+"""GPU parity of the whole layer (moe_forward) against the oracle on small
+layers, in bf16 and FP8, with device and host buffers.
+
+Error measure for layer outputs: per token row, max |y - y_ref| / max |y_ref|
+against the fp32 oracle, at most 2e-2 (bf16) and 4e-2 (FP8); rows whose
+reference is exactly zero (all slots sentinel) must be exactly zero."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from grouped_gemm_serving_gb300 import synth
+from tests.gpu_helpers import dev, dev_bf16, host, host_f32_from_bf16, require_gpu, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "fp8": 4e-2}
+
+
+@pytest.fixture(scope="module")
+def moe():
+    require_gpu()
+    from grouped_gemm_serving_gb300 import moe as m
+    return m
+
+
+def quantised_weights(moe, W):
+    """bf16 bits [E, N, K] -> device e4m3 + scales through the library's quantiser."""
+    E, N, K = W.shape
+    q = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+    s = torch.empty((E, (N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    moe.moe_weight_quant_fp8(dev_bf16(W), E, N, K, q, s)
+    return q, s
+
+
+def run_forward(moe, wl, x, W1, W2, W1s=None, W2s=None, host_io=False, logits=None, bias=None, mask=None):
+    fp8 = W1s is not None
+    T, H = wl.T, wl.H
+    ids = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
+    if host_io:
+        xin = torch.from_numpy(x.view(np.int16)).pin_memory()
+        lin = torch.from_numpy(logits).pin_memory()
+        out = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    else:
+        xin, lin = dev_bf16(x), dev(logits)
+        out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    a = moe.forward_args(dtype=moe.MOE_FP8_E4M3_B128 if fp8 else moe.MOE_BF16, T=T, E=wl.E, k=wl.k, H=H,
+                         I=wl.I, x=xin, W1=W1, W2=W2, W1_scales=W1s, W2_scales=W2s, out=out, logits=lin,
+                         expert_bias=None if bias is None else dev(bias),
+                         sentinel_mask=None if mask is None else dev(mask), topk_ids=ids, topk_w=w,
+                         renormalize=wl.renormalize, host_io=host_io)
+    nbytes = moe.moe_forward_workspace_size(a)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    moe.moe_forward(a, ws, nbytes)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    y = out.view(torch.bfloat16).float().cpu().numpy() if host_io else host_f32_from_bf16(out.view(torch.bfloat16))
+    return y, host(ids), host(w)
+
+
+LAYERS = [
+    synth.WORKLOADS["tiny-8e-top2"],
+    synth.Workload("mid-16e-top4", T=300, E=16, k=4, H=256, I=384, n_sentinel=40, bias="normal0.5"),
+    synth.Workload("ragged-12e-top3", T=97, E=12, k=3, H=136, I=200, n_sentinel=5),
+]
+
+
+@pytest.mark.parametrize("wl", LAYERS, ids=lambda w: w.name)
+def test_forward_bf16(moe, wl):
+    x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    logits, bias, mask = synth.router_logits(wl), synth.expert_bias(wl), synth.sentinel_mask(wl)
+    ref = oracle.moe_forward(x, W1, W2, E=wl.E, k=wl.k, logits=logits, bias=bias, sentinel_mask=mask)
+    y, ids, w = run_forward(moe, wl, x, dev_bf16(W1), dev_bf16(W2), logits=logits, bias=bias, mask=mask)
+    assert np.array_equal(ids, ref["ids"])
+    err = row_rel_err(y, ref["out"])
+    assert err.max() <= TOL["bf16"], err.max()
+    dead = (ref["ids"] == wl.E).all(axis=1)
+    assert np.all(y[dead] == 0)
+
+
+@pytest.mark.parametrize("wl", [LAYERS[0], synth.Workload("fp8-16e-top4", T=200, E=16, k=4, H=256, I=384,
+                                                          n_sentinel=30)], ids=lambda w: w.name)
+def test_forward_fp8(moe, wl):
+    x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    logits, mask = synth.router_logits(wl), synth.sentinel_mask(wl)
+    q1, s1 = oracle.quant_weight_fp8(W1)
+    q2, s2 = oracle.quant_weight_fp8(W2)
+    ref = oracle.moe_forward(x, q1, q2, W1_scales=s1, W2_scales=s2, E=wl.E, k=wl.k, logits=logits,
+                             sentinel_mask=mask)
+    dq1, ds1 = quantised_weights(moe, W1)
+    dq2, ds2 = quantised_weights(moe, W2)
+    assert np.array_equal(host(dq1), q1) and np.array_equal(host(ds2), s2)
+    y, ids, _ = run_forward(moe, wl, x, dq1, dq2, ds1, ds2, logits=logits, mask=mask)
+    assert np.array_equal(ids, ref["ids"])
+    err = row_rel_err(y, ref["out"])
+    assert err.max() <= TOL["fp8"], err.max()
+
+
+def test_forward_host_io_equals_device_path(moe):
+    wl = LAYERS[1]
+    x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    logits = synth.router_logits(wl)
+    d1, d2 = dev_bf16(W1), dev_bf16(W2)
+    y_dev, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits)
+    y_host, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits, host_io=True)
+    assert np.array_equal(y_dev, y_host)
+    y_again, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits)
+    assert np.array_equal(y_dev, y_again)                     # bit-reproducible

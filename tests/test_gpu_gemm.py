@@ -1,0 +1,142 @@
+"""GPU parity of the tcgen05 grouped GEMM (bf16 and block-scaled FP8; store,
+SwiGLU and SwiGLU+FP8-quantising epilogues) against the CPU oracle.
+
+Shapes span several row and column tiles with ragged tails: experts with 0,
+a few and more than 128 rows, N and K that are not multiples of the tile,
+sentinel rows NaN-poisoned on input and checked to be exact zeros on output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from grouped_gemm_serving_gb300 import synth
+from grouped_gemm_serving_gb300.synth import bf16_bits_to_f32
+from tests.gpu_helpers import (assert_close_bf16, dev, dev_bf16, host, host_bf16_bits,
+                               host_f32_from_bf16, require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    require_gpu()
+    from grouped_gemm_serving_gb300 import moe as m
+    return m
+
+
+def _weights(E, N, K, seed, std=0.05):
+    return np.stack([synth.dense_rows(N, K, seed * 1000 + e, std=std, tensor_id=4) for e in range(E)])
+
+
+BF16_CASES = [
+    # E, M_cap, live, N, K, empty experts
+    (4, 300, 260, 264, 200, 1),
+    (8, 1100, 1000, 512, 136, 2),
+    (3, 129, 129, 256, 64, 0),
+    (16, 2048, 1500, 2880, 256, 3),
+]
+
+
+@pytest.mark.parametrize("E,M_cap,live,N,K,n_empty", BF16_CASES)
+def test_bf16_store(moe, E, M_cap, live, N, K, n_empty):
+    off = synth.grouped_offsets(E, live, seed=E + K, empty_experts=n_empty)
+    A = synth.grouped_rows(M_cap, K, live, seed=N)
+    B = _weights(E, N, K, 1)
+    ref = oracle.grouped_gemm_bf16(A, B, off)
+    C = torch.full((M_cap, N), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, dev_bf16(A), None, dev_bf16(B), None, dev(off), E, M_cap, N, K,
+                         moe.MOE_EPI_STORE, C, None)
+    assert moe.moe_get_device_error() == 0
+    got = host_f32_from_bf16(C)
+    assert_close_bf16(got[:live], ref[:live])
+    assert np.all(host_bf16_bits(C)[live:] == 0)
+
+
+@pytest.mark.parametrize("E,M_cap,live,I,K,n_empty", [
+    (4, 300, 260, 200, 200, 1), (8, 1100, 1000, 256, 128, 2), (5, 700, 640, 2880, 192, 0),
+    (2, 256, 256, 72, 64, 0)])
+def test_bf16_swiglu(moe, E, M_cap, live, I, K, n_empty):
+    off = synth.grouped_offsets(E, live, seed=E * 7 + K, empty_experts=n_empty)
+    A = synth.grouped_rows(M_cap, K, live, seed=I)
+    B = _weights(E, 2 * I, K, 2)
+    ref = oracle.swiglu(oracle.grouped_gemm_bf16(A, B, off), live)
+    h = torch.full((M_cap, I), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, dev_bf16(A), None, dev_bf16(B), None, dev(off), E, M_cap, 2 * I, K,
+                         moe.MOE_EPI_SWIGLU, h, None)
+    assert moe.moe_get_device_error() == 0
+    got = host_f32_from_bf16(h)
+    assert_close_bf16(got[:live], ref[:live])
+    assert np.all(host_bf16_bits(h)[live:] == 0)
+
+
+def _fp8_operands(E, M_cap, live, N, K, seed):
+    off = synth.grouped_offsets(E, live, seed=seed, empty_experts=1 if E > 2 else 0)
+    A = synth.grouped_rows(M_cap, K, live, seed=seed + 1)
+    A[live:] = 0                                      # quantisation of NaN rows is undefined
+    qa, sa = oracle.quant_act_fp8(A)
+    qb, sb = oracle.quant_weight_fp8(_weights(E, N, K, seed + 2))
+    return off, qa, sa, qb, sb
+
+
+@pytest.mark.parametrize("E,M_cap,live,N,K", [(4, 300, 260, 512, 256), (8, 1000, 900, 384, 512),
+                                             (3, 200, 200, 264, 128)])
+def test_fp8_store(moe, E, M_cap, live, N, K):
+    off, qa, sa, qb, sb = _fp8_operands(E, M_cap, live, N, K, 5)
+    ref = oracle.grouped_gemm_fp8(qa, sa, qb, sb, off)
+    C = torch.full((M_cap, N), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, dev(qa), dev(np.ascontiguousarray(sa.T)), dev(qb), dev(sb),
+                         dev(off), E, M_cap, N, K, moe.MOE_EPI_STORE, C, None)
+    assert moe.moe_get_device_error() == 0
+    got = host_f32_from_bf16(C)
+    assert_close_bf16(got[:live], ref[:live], rtol=2.0 ** -7, row_atol=2e-3)
+    assert np.all(host_bf16_bits(C)[live:] == 0)
+
+
+@pytest.mark.parametrize("E,M_cap,live,I,K", [(4, 300, 260, 256, 256), (6, 900, 800, 384, 384)])
+def test_fp8_swiglu_and_quantising_epilogue(moe, E, M_cap, live, I, K):
+    off, qa, sa, qb, sb = _fp8_operands(E, M_cap, live, 2 * I, K, 9)
+    ref_h = oracle.swiglu(oracle.grouped_gemm_fp8(qa, sa, qb, sb, off), live)
+    args = (dev(qa), dev(np.ascontiguousarray(sa.T)), dev(qb), dev(sb), dev(off), E, M_cap, 2 * I, K)
+    h = torch.empty((M_cap, I), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_SWIGLU, h, None)
+    hq = torch.full((M_cap, I), 7, dtype=torch.uint8, device="cuda")
+    hs = torch.full((I // 128, M_cap), -1.0, dtype=torch.float32, device="cuda")
+    moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_SWIGLU_QUANT_FP8, hq, hs)
+    assert moe.moe_get_device_error() == 0
+    got_h = host_f32_from_bf16(h)
+    assert_close_bf16(got_h[:live], ref_h[:live], rtol=2.0 ** -7, row_atol=2e-3)
+    # the fused quantisation equals the standalone quantiser applied to the
+    # bf16 h of the SwiGLU epilogue (same accumulators, same rounding)
+    q2 = torch.empty((M_cap, I), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty((M_cap, I // 128), dtype=torch.float32, device="cuda")
+    moe.moe_act_quant_fp8(h, M_cap, I, q2, s2)
+    assert np.array_equal(host(hq)[:live], host(q2)[:live])
+    assert np.array_equal(host(hs).T[:live], host(s2)[:live])
+    # against the oracle: dequantised h within the e4m3 rounding of the oracle's h
+    deq = oracle.e4m3_decode(host(hq)).reshape(M_cap, I // 128, 128) * host(hs).T[:, :, None]
+    assert_close_bf16(deq.reshape(M_cap, I)[:live], ref_h[:live], rtol=2.0 ** -4 + 2.0 ** -7, row_atol=4e-3)
+    # sentinel rows: code 0 and scale 1
+    assert np.all(host(hq)[live:] == 0) and np.all(host(hs).T[live:] == 1.0)
+
+
+def test_invalid_offsets_skip_the_gemm(moe):
+    E, M_cap, N, K = 4, 256, 256, 64
+    off = np.array([0, 100, 90, 200, 250], np.int32)
+    A = torch.zeros((M_cap, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((E, N, K), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((M_cap, N), 9, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, A, None, B, None, dev(off), E, M_cap, N, K, moe.MOE_EPI_STORE, C, None)
+    assert moe.moe_get_device_error() == moe.MOE_DEVERR_OFFSETS
+    assert np.all(host_bf16_bits(C).view(np.int16) == 9)
+
+
+def test_deterministic(moe):
+    E, M_cap, live, N, K = 8, 1100, 1000, 512, 256
+    off = synth.grouped_offsets(E, live, seed=3)
+    A, B = dev_bf16(synth.grouped_rows(M_cap, K, live, seed=4)), dev_bf16(_weights(E, N, K, 3))
+    outs = []
+    for _ in range(2):
+        C = torch.empty((M_cap, N), dtype=torch.bfloat16, device="cuda")
+        moe.moe_grouped_gemm(moe.MOE_BF16, A, None, B, None, dev(off), E, M_cap, N, K, moe.MOE_EPI_STORE, C, None)
+        outs.append(host_bf16_bits(C))
+    assert np.array_equal(outs[0], outs[1])
