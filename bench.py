@@ -1,0 +1,463 @@
+"""Benchmark of the MoE expert layer on GB300.
+
+One step = one pass of the whole hot path over one batch: route + sort,
+permute, grouped GEMM gate_up with fused SwiGLU, grouped GEMM down, weighted
+combine (FP8 workloads add the activation quantiser and use the quantising
+epilogue).  Default workload: the 32-expert top-4 layer (T=4096, H=I=2880,
+bf16, biased routing).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle (a deliberately plain program) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; grouped-GEMM TFLOP/s as % of GB300 tensor peak"
+DEFAULT_WORKLOAD = "32e-top4-h2880"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, v in enumerate(flags) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ inputs
+def make_layer(wl, torch, moe, synth):
+    """Seeded synthetic layer resident on the device (weights drawn on the host
+    expert by expert, copied once; FP8 weights quantised by the library)."""
+    t0 = time.time()
+    dev = torch.device("cuda")
+
+    def bf16_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    L = {}
+    L["x_host"] = synth.hidden_states(wl)
+    L["logits_host"] = synth.router_logits(wl)
+    bias = synth.expert_bias(wl)
+    L["bias_host"] = bias
+    L["x"] = bf16_dev(L["x_host"])
+    L["logits"] = torch.from_numpy(L["logits_host"]).to(dev)
+    L["bias"] = None if bias is None else torch.from_numpy(bias).to(dev)
+    fp8 = wl.dtype == "fp8"
+    for which, (n, kdim) in (("w1", (2 * wl.I, wl.H)), ("w2", (wl.H, wl.I))):
+        if not fp8:
+            L[which] = bf16_dev(synth.expert_weights(wl, which))
+            continue
+        q = torch.empty((wl.E, n, kdim), dtype=torch.uint8, device=dev)
+        s = torch.empty((wl.E, (n + 127) // 128, kdim // 128), dtype=torch.float32, device=dev)
+        chunk = 16
+        for e0 in range(0, wl.E, chunk):
+            ex = list(range(e0, min(wl.E, e0 + chunk)))
+            wb = bf16_dev(synth.expert_weights(wl, which, experts=ex))
+            moe.moe_weight_quant_fp8(wb, len(ex), n, kdim, q[e0:e0 + len(ex)], s[e0:e0 + len(ex)])
+            torch.cuda.synchronize()
+            del wb
+        L[which], L[which + "_s"] = q, s
+    L["setup_s"] = time.time() - t0
+    return L
+
+
+class Step:
+    """The hot path as the chain of C-ABI calls moe_forward enqueues, with
+    CUDA events between kernels on the launching stream."""
+
+    def __init__(self, wl, L, torch, moe):
+        self.wl, self.L, self.torch, self.moe = wl, L, torch, moe
+        T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
+        R = T * k
+        self.fp8 = wl.dtype == "fp8"
+        dev = torch.device("cuda")
+        z = lambda *s, dt=torch.uint8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        self.ids, self.w = z(T, k, dt=torch.int32), z(T, k, dt=torch.float32)
+        self.sr, self.rp, self.off = z(R, dt=torch.int32), z(R, dt=torch.int32), z(E + 1, dt=torch.int32)
+        self.rws_bytes = moe.moe_route_sort_workspace_size(T, E, k)
+        self.rws = z(max(self.rws_bytes, 16))
+        if self.fp8:
+            self.xq, self.xs = z(T, H), z(T, H // 128, dt=torch.float32)
+            self.xp, self.xps = z(R, H), z(H // 128, R, dt=torch.float32)
+            self.h, self.hs = z(R, I), z(I // 128, R, dt=torch.float32)
+        else:
+            self.xp, self.h = z(R, H, dt=torch.bfloat16), z(R, I, dt=torch.bfloat16)
+        self.y2 = z(R, H, dt=torch.bfloat16)
+        self.out = z(T, H, dt=torch.bfloat16)
+        self.names = (["route_sort"] + (["act_quant"] if self.fp8 else []) +
+                      ["permute", "gemm_gate_up_swiglu", "gemm_down", "combine"])
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(self.names) + 1)]
+        self.times = {n: [] for n in self.names}
+
+    def launches_per_step(self):
+        return len(self.names) + 1   # route_sort runs two kernels
+
+    def run(self, record=False):
+        wl, L, moe = self.wl, self.L, self.moe
+        T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
+        R = T * k
+        ev = iter(self.ev)
+        mark = (lambda: next(ev).record()) if record else (lambda: None)
+        mark()
+        moe.moe_route_sort(L["logits"], L["bias"], None, self.ids, self.w, T, E, k, wl.renormalize,
+                           self.sr, self.rp, self.off, self.rws, self.rws_bytes)
+        mark()
+        if self.fp8:
+            moe.moe_act_quant_fp8(L["x"], T, H, self.xq, self.xs)
+            mark()
+            moe.moe_permute(moe.MOE_FP8_E4M3_B128, self.xq, self.xs, T, H, k, self.sr, self.off, E, R,
+                            self.xp, self.xps)
+            mark()
+            moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, self.xp, self.xps, L["w1"], L["w1_s"], self.off, E, R,
+                                 2 * I, H, moe.MOE_EPI_SWIGLU_QUANT_FP8, self.h, self.hs)
+            mark()
+            moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, self.h, self.hs, L["w2"], L["w2_s"], self.off, E, R,
+                                 H, I, moe.MOE_EPI_STORE, self.y2, None)
+        else:
+            moe.moe_permute(moe.MOE_BF16, L["x"], None, T, H, k, self.sr, self.off, E, R, self.xp, None)
+            mark()
+            moe.moe_grouped_gemm(moe.MOE_BF16, self.xp, None, L["w1"], None, self.off, E, R, 2 * I, H,
+                                 moe.MOE_EPI_SWIGLU, self.h, None)
+            mark()
+            moe.moe_grouped_gemm(moe.MOE_BF16, self.h, None, L["w2"], None, self.off, E, R, H, I,
+                                 moe.MOE_EPI_STORE, self.y2, None)
+        mark()
+        moe.moe_combine(self.y2, self.ids, self.w, self.rp, T, k, H, E, self.out)
+        mark()
+
+    def collect(self):
+        for i, n in enumerate(self.names):
+            self.times[n].append(self.ev[i].elapsed_time(self.ev[i + 1]))
+        return self.ev[0].elapsed_time(self.ev[-1])
+
+
+def flops_bytes(wl, live_rows, experts_live):
+    """Algorithmic work of one step: GEMM FLOPs on live rows and the minimum
+    HBM bytes of each kernel (weights of experts with rows, activations once)."""
+    T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
+    R = T * k
+    wb = 1 if wl.dtype == "fp8" else 2
+    ab = 1 if wl.dtype == "fp8" else 2
+    f1 = 2.0 * live_rows * (2 * I) * H
+    f2 = 2.0 * live_rows * H * I
+    b1 = experts_live * 2 * I * H * wb + live_rows * H * ab + live_rows * I * ab
+    b2 = experts_live * H * I * wb + live_rows * I * ab + R * H * 2
+    bp = T * H * ab + live_rows * H * ab
+    bc = live_rows * H * 2 + R * 12 + T * H * 2
+    return dict(gemm1_flop=f1, gemm2_flop=f2, gemm1_bytes=b1, gemm2_bytes=b2, permute_bytes=bp,
+                combine_bytes=bc)
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_tokens_per_s(wl, sample_tokens, x_host, logits_host, bias_host, W1, W2, W1s=None, W2s=None):
+    import oracle
+    xs = x_host[:sample_tokens]
+    ls = logits_host[:sample_tokens]
+    t0 = time.perf_counter()
+    oracle.moe_forward(xs, W1, W2, E=wl.E, k=wl.k, logits=ls, bias=bias_host,
+                       renormalize=wl.renormalize, W1_scales=W1s, W2_scales=W2s)
+    dt = time.perf_counter() - t0
+    return sample_tokens / dt, dt
+
+
+def cpu_info():
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return cores, model
+
+
+def host_weights(wl, synth):
+    W1 = synth.expert_weights(wl, "w1")
+    W2 = synth.expert_weights(wl, "w2")
+    if wl.dtype != "fp8":
+        return W1, W2, None, None
+    import oracle
+    q1, s1 = oracle.quant_weight_fp8(W1)
+    q2, s2 = oracle.quant_weight_fp8(W2)
+    return q1, q2, s1, s2
+
+
+def reference_main(args, wl, synth):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    W1, W2, s1, s2 = host_weights(wl, synth)
+    x, logits, bias = synth.hidden_states(wl), synth.router_logits(wl), synth.expert_bias(wl)
+    per_step = max(1, min(args.cpu_sample_tokens, 4))
+    for i in range(args.warmup):
+        oracle_tokens_per_s(wl, per_step, x[i * per_step:], logits[i * per_step:], bias, W1, W2, s1, s2)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        j = (i * per_step) % max(1, wl.T - per_step)
+        oracle_tokens_per_s(wl, per_step, x[j:], logits[j:], bias, W1, W2, s1, s2)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    cores, model = cpu_info()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy draws)",
+        "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I,
+                   "layer_dtype": wl.dtype, "step": f"{per_step} tokens of the workload per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} tokens per step x {args.steps} steps of {wl.name}",
+                         "cpu": model, "host_cores": cores},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse()
+    from grouped_gemm_serving_gb300 import synth
+    if args.workload in synth.WORKLOADS:
+        wl = synth.WORKLOADS[args.workload]
+    else:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.WORKLOADS)}")
+    if args.impl == "reference":
+        return reference_main(args, wl, synth)
+
+    import torch
+    from grouped_gemm_serving_gb300 import build as gbuild
+    gbuild.build()
+    from grouped_gemm_serving_gb300 import moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    L = make_layer(wl, torch, moe, synth)
+    step = Step(wl, L, torch, moe)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for i in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    # ---- timed region: K steps, L2 flushed between steps (untimed)
+    barrier()
+    torch.cuda.synchronize()
+    step_ms = []
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step.run(record=True)
+            torch.cuda.synchronize()
+            step_ms.append(step.collect())
+        wall = time.perf_counter() - wall0
+    torch.cuda.synchronize()
+    barrier()
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit("device error in the timed region")
+    ms = statistics.fmean(step_ms)
+    ms_t = torch.tensor([ms], device="cuda")
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    # ---- e2e: moe_forward with host buffers (pinned), copies inside the timed region
+    x_pin = torch.from_numpy(L["x_host"].view(np.int16)).pin_memory()
+    lg_pin = torch.from_numpy(L["logits_host"]).pin_memory()
+    out_pin = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    fa = moe.forward_args(dtype=moe.MOE_FP8_E4M3_B128 if wl.dtype == "fp8" else moe.MOE_BF16, T=wl.T, E=wl.E,
+                          k=wl.k, H=wl.H, I=wl.I, x=x_pin, W1=L["w1"], W2=L["w2"], W1_scales=L.get("w1_s"),
+                          W2_scales=L.get("w2_s"), out=out_pin, logits=lg_pin, expert_bias=L["bias"],
+                          renormalize=wl.renormalize, host_io=True)
+    nws = moe.moe_forward_workspace_size(fa)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        moe.moe_forward(fa, ws, nws)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0.record()
+        moe.moe_forward(fa, ws, nws)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_mean = statistics.fmean(e2e_ms)
+    e2e_t = torch.tensor([e2e_mean], device="cuda")
+    if dist is not None:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit("device error in the e2e region")
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (the gate_up grouped GEMM)
+    off = step.off.cpu().numpy()
+    live = int(off[-1])
+    experts_live = int((np.diff(off) > 0).sum())
+    fb = flops_bytes(wl, live, experts_live)
+    kt = {n: statistics.fmean(v) for n, v in step.times.items()}
+    pk, pk_kind = peaks()
+    g1 = kt["gemm_gate_up_swiglu"]
+    g2 = kt["gemm_down"]
+    if wl.dtype == "fp8":
+        peak = pk["bf16_tflops"] * 2.0        # fp8 dense = 2 x bf16 (nominal ratio)
+        peak_note = f"fp8 = 2 x {pk_kind} bf16 burst"
+    else:
+        peak = pk["bf16_tflops"]
+        peak_note = f"{pk_kind} bf16 burst (cuBLAS)"
+    ach1 = fb["gemm1_flop"] / (g1 * 1e-3) / 1e12
+    ach2 = fb["gemm2_flop"] / (g2 * 1e-3) / 1e12
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            traffic = json.load(f).get("gemm_gate_up_swiglu_bytes")
+    tokens = wl.T * world
+    cores, model = cpu_info()
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        W1, W2, s1, s2 = host_weights(wl, synth)
+        n = args.cpu_sample_tokens if wl.dtype != "fp8" else max(1, args.cpu_sample_tokens // 8)
+        v, dt = oracle_tokens_per_s(wl, n, L["x_host"], L["logits_host"], L["bias_host"], W1, W2, s1, s2)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n} of {wl.T} tokens of {wl.name} ({dt:.1f} s)", "cpu": model,
+               "host_cores": cores}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": tokens / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if wl.dtype == "fp8" else "bf16",
+        "data": "synthetic (seeded numpy draws; random-init weights N(0,0.02))",
+        "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I,
+                   "bias": wl.bias, "live_rows": live, "experts_with_rows": experts_live,
+                   "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+        "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate_up + fused SwiGLU",
+                     "achieved": ach1, "peak": peak, "unit": "TFLOP/s", "frac": ach1 / peak,
+                     "peak_source": peak_note, "traffic": traffic,
+                     "algorithmic_flop": fb["gemm1_flop"], "algorithmic_bytes": fb["gemm1_bytes"]},
+        "gemm": {"gate_up_tflops": ach1, "down_tflops": ach2, "gate_up_frac": ach1 / peak,
+                 "down_frac": ach2 / peak,
+                 "pair_tflops": (fb["gemm1_flop"] + fb["gemm2_flop"]) / ((g1 + g2) * 1e-3) / 1e12},
+        "kernels_ms": kt,
+        "hbm": {"permute_gbs": fb["permute_bytes"] / (kt["permute"] * 1e-3) / 1e9,
+                "combine_gbs": fb["combine_bytes"] / (kt["combine"] * 1e-3) / 1e9,
+                "peak_gbs": pk["hbm_gbs"]},
+        "e2e": {"value": tokens / (float(e2e_t.item()) * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
+                "d2h_bytes_per_step": wl.T * wl.H * 2},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "wall_s_timed": wall,
+        "setup_s": L["setup_s"],
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -191,7 +191,11 @@ def route_sort_t(E: int, k: int, *, logits=None, expert_bias=None, sentinel_mask
 def forward_args(*, dtype, T, E, k, H, I, x, W1, W2, out, logits=None, expert_bias=None,
                  sentinel_mask=None, topk_ids=None, topk_w=None, W1_scales=None, W2_scales=None,
                  renormalize=True, host_io=False) -> ForwardArgs:
+    """Fill a ForwardArgs from tensors (or raw addresses).  The returned
+    struct keeps the given tensors alive for as long as it lives."""
     a = ForwardArgs()
+    a._keepalive = [logits, expert_bias, sentinel_mask, topk_ids, topk_w, x, W1, W1_scales, W2,
+                    W2_scales, out]
     a.dtype, a.T, a.E, a.k, a.H, a.I = dtype, T, E, k, H, I
     a.renormalize = int(renormalize)
     a.flags = MOE_FWD_HOST_IO if host_io else 0
