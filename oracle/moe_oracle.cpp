@@ -86,6 +86,18 @@ uint8_t e4m3_encode(float v) {
     return sign | static_cast<uint8_t>(((eu + 7) << 3) | (static_cast<int>(m) - 8));
 }
 
+// The 256 decoded values, filled once from e4m3_decode (same values; only
+// saves re-deriving them inside the GEMM loops).
+const float* e4m3_table() {
+    static float table[256];
+    static bool ready = [] {
+        for (int c = 0; c < 256; ++c) table[c] = e4m3_decode(static_cast<uint8_t>(c));
+        return true;
+    }();
+    (void)ready;
+    return table;
+}
+
 // amax / 448 in fp32; a group or block of zeros gets scale 1.
 inline float fp8_scale_from_amax(float amax) {
     return amax == 0.0f ? 1.0f : amax / kE4M3Max;
@@ -292,14 +304,15 @@ void orc_grouped_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb,
             for (int n = 0; n < N; ++n) Ci[n] = 0.0f;
             continue;
         }
-        for (int c = 0; c < K; ++c) a[c] = e4m3_decode(qa[p * K + c]);
+        const float* dec = e4m3_table();
+        for (int c = 0; c < K; ++c) a[c] = dec[qa[p * K + c]];
         const uint8_t* Be = qb + (int64_t)e * N * K;
         for (int n = 0; n < N; ++n) {
             double acc = 0.0;
             for (int kb = 0; kb < KB; ++kb) {
                 double part = 0.0;
                 for (int c = kb * 128; c < kb * 128 + 128; ++c)
-                    part += (double)a[c] * (double)e4m3_decode(Be[(int64_t)n * K + c]);
+                    part += (double)a[c] * (double)dec[Be[(int64_t)n * K + c]];
                 acc += (double)sa[p * KB + kb] * (double)sb[((int64_t)e * NB + n / 128) * KB + kb] * part;
             }
             Ci[n] = static_cast<float>(acc);
