@@ -17,7 +17,9 @@
 //                       then a stable in-order rank of every slot from
 //                       per-warp match_any peer masks.  Writes sorted_rows,
 //                       row_pos and (block 0) offsets.
+#include <atomic>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -265,6 +267,74 @@ extern "C" moe_status_t moe_route_sort(const float* logits, const float* expert_
     const SortGeometry g = geometry(T, k);
     int* counts = static_cast<int*>(ws);
     MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(g.blocks) * (E + 1) * sizeof(int), s));
+    route_topk_hist<<<(T + kWarps - 1) / kWarps, kThreads, 0, s>>>(
+        logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
+        renormalize, g.slots_per_block, counts, err);
+    MOE_CHECK_LAUNCH();
+    route_scatter<<<g.blocks, kThreads, 0, s>>>(topk_ids, static_cast<int64_t>(T) * k, E,
+                                                g.slots_per_block, g.blocks, counts, sorted_rows,
+                                                row_pos, offsets, err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  The per-sort-block histogram lives in a static
+// device array instead of caller workspace, for callers that may not allocate
+// device memory themselves (see moe_route_sort_noalloc in moe.h).
+namespace {
+
+constexpr size_t kStaticScratchBytes = 256 * 1024;
+constexpr size_t kStaticScratchInts = kStaticScratchBytes / sizeof(int);
+static __device__ __align__(256) int g_route_scratch[kStaticScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::atomic<int*> g_route_scratch_ptr[kMaxDevices];
+std::mutex g_route_scratch_mu;
+
+// Device address of g_route_scratch on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, not a device address).
+int* static_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    int* p = g_route_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    std::lock_guard<std::mutex> lk(g_route_scratch_mu);
+    p = g_route_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_route_scratch) != cudaSuccess || !addr) return nullptr;
+        p = static_cast<int*>(addr);
+        g_route_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_route_sort_noalloc(const float* logits, const float* expert_bias,
+                                               const uint8_t* sentinel_mask, int32_t* topk_ids,
+                                               float* topk_w, int T, int E, int k, int renormalize,
+                                               int32_t* sorted_rows, int32_t* row_pos,
+                                               int32_t* offsets, moe_stream_t stream) {
+    MOE_CHECK_ARG(T >= 1 && E >= 1 && E <= kMaxE && k >= 1 && k <= E && k <= kMaxK);
+    MOE_CHECK_ARG(static_cast<int64_t>(T) * k < INT_MAX);
+    MOE_CHECK_ARG(topk_ids && sorted_rows && row_pos && offsets);
+    MOE_CHECK_ARG(!logits || topk_w);
+    MOE_CHECK_ARG(moe::aligned16(topk_ids) && moe::aligned16(sorted_rows) &&
+                  moe::aligned16(row_pos) && moe::aligned16(offsets));
+    MOE_CHECK_ARG(!logits || (moe::aligned16(logits) && moe::aligned16(topk_w)));
+    MOE_CHECK_ARG(!expert_bias || moe::aligned16(expert_bias));
+    const SortGeometry g = geometry(T, k);
+    const size_t ints = static_cast<size_t>(g.blocks) * (E + 1);
+    if (ints > kStaticScratchInts) return MOE_ERR_WORKSPACE;   // beyond the static scratch
+    int* counts = static_scratch();
+    if (!counts) return MOE_ERR_CUDA;
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, ints * sizeof(int), s));
     route_topk_hist<<<(T + kWarps - 1) / kWarps, kThreads, 0, s>>>(
         logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
         renormalize, g.slots_per_block, counts, err);

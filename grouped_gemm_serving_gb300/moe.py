@@ -47,6 +47,7 @@ _SIGS = {
     "moe_get_device_error": (_S, [_P, _P]),
     "moe_route_sort_workspace_size": (_Z, [_I, _I, _I]),
     "moe_route_sort": (_S, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_route_sort_noalloc": (_S, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_act_quant_fp8": (_S, [_P, _I, _I, _P, _P, _P]),
     "moe_weight_quant_fp8": (_S, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_S, [_I, _P, _P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
@@ -125,6 +126,16 @@ def moe_route_sort(logits, expert_bias, sentinel_mask, topk_ids, topk_w, T, E, k
     _check(lib().moe_route_sort(_p(logits), _p(expert_bias), _p(sentinel_mask), _p(topk_ids),
                                 _p(topk_w), T, E, k, int(renormalize), _p(sorted_rows), _p(row_pos),
                                 _p(offsets), _p(ws), ws_bytes, _stream(stream)), "moe_route_sort")
+
+
+def moe_route_sort_noalloc(logits, expert_bias, sentinel_mask, topk_ids, topk_w, T, E, k, renormalize,
+                           sorted_rows, row_pos, offsets, stream=None):
+    """moe_route_sort with the histogram scratch in the library's static
+    device array: for callers that cannot allocate device memory."""
+    _check(lib().moe_route_sort_noalloc(_p(logits), _p(expert_bias), _p(sentinel_mask), _p(topk_ids),
+                                        _p(topk_w), T, E, k, int(renormalize), _p(sorted_rows),
+                                        _p(row_pos), _p(offsets), _stream(stream)),
+           "moe_route_sort_noalloc")
 
 
 def moe_act_quant_fp8(x, M, K, q, scales, stream=None):

@@ -128,6 +128,34 @@ moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
                             moe_stream_t stream);
 
 /*
+ * moe_route_sort_noalloc -- moe_route_sort without caller workspace.  The
+ * paper has no counterpart: this entry point exists for callers that
+ * cannot allocate device memory themselves, such as a plug-in running inside
+ * a serving engine that reserves and owns the whole device memory pool, or a
+ * latency-critical path where an allocation call (which may synchronise the
+ * device) is not allowed.
+ *
+ * Same arguments, results and limits as moe_route_sort, minus ws/ws_bytes.
+ * The per-sort-block histogram lives in a static device array of 256 KiB
+ * inside libmoe.so (present on every GPU that loads the library, until the
+ * process exits).  It holds blocks * (E + 1) 32-bit counters, where
+ * blocks = ceil(T / floor(2048 / k)); a request that needs more returns
+ * MOE_ERR_WORKSPACE with nothing enqueued (for example E = 256 allows up to
+ * 255 blocks, about 522 thousand slots at k = 8).
+ * The call allocates and frees nothing.  On its first call on a device it
+ * looks up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  Each call clears
+ * the counters it uses on `stream` before use.  All calls share the one
+ * array: calls whose work overlaps on the GPU (different streams without
+ * ordering between them) race on it and give wrong results.
+ */
+moe_status_t moe_route_sort_noalloc(const float* logits, const float* expert_bias,
+                                    const uint8_t* sentinel_mask, int32_t* topk_ids,
+                                    float* topk_w, int T, int E, int k, int renormalize,
+                                    int32_t* sorted_rows, int32_t* row_pos, int32_t* offsets,
+                                    moe_stream_t stream);
+
+/*
  * moe_act_quant_fp8 -- per-token activation quantisation (fp8_act_quant /
  * per_token_cast_to_fp8 of section 1 of the transformers MoE/FP8 write-up).
  * For row m and 128-column group g: s = amax(|x[m, g*128 : g*128+128]|) / 448
