@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="shrink the workload to this many experts, tokens scaled alike "
+                         "(same rows per expert; for small profiler captures)")
     return ap.parse_args()
 
 
@@ -298,14 +301,98 @@ def reference_main(args, wl, synth):
     return 0
 
 
+# ------------------------------------------------------------------ sweep
+def sweep_main(args, synth, torch, moe):
+    """Both grouped GEMMs over 16384 permuted rows of 128 experts (H=2048,
+    I=768, bf16) with 100 / 50 / 12.5 % of the rows live: split equally over
+    all experts, and concentrated on the first live/128 experts (128 rows
+    each).  Sentinel rows are NaN on input; the GEMMs write them as zeros."""
+    pk, pk_kind = peaks()
+    base = synth.Sweep()
+    wl = base.workload
+
+    def bf16_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+
+    W1 = bf16_dev(synth.expert_weights(wl, "w1"))
+    W2 = bf16_dev(synth.expert_weights(wl, "w2"))
+    M, E, H, I = base.M_cap, base.E, base.H, base.I
+    h = torch.empty((M, I), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    rows = []
+    for live in (16384, 8192, 2048):
+        sw = synth.Sweep(live=live)
+        A = bf16_dev(synth.sweep_rows(sw))
+        for layout in ("equal", "concentrated"):
+            if layout == "equal":
+                off_np = synth.sweep_offsets(sw)
+            else:
+                n_exp = live // 128
+                off_np = np.minimum(np.arange(E + 1) * 128, live).astype(np.int32)
+                assert off_np[n_exp] == live
+            off = torch.from_numpy(off_np).cuda()
+
+            def run():
+                moe.moe_grouped_gemm(moe.MOE_BF16, A, None, W1, None, off, E, M, 2 * I, H, moe.MOE_EPI_SWIGLU,
+                                     h, None)
+                ev[1].record()
+                moe.moe_grouped_gemm(moe.MOE_BF16, h, None, W2, None, off, E, M, H, I, moe.MOE_EPI_STORE, y2,
+                                     None)
+
+            for _ in range(max(3, args.warmup)):
+                run()
+            torch.cuda.synchronize()
+            t1, t2 = [], []
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                ev[0].record()
+                run()
+                ev[2].record()
+                torch.cuda.synchronize()
+                t1.append(ev[0].elapsed_time(ev[1]))
+                t2.append(ev[1].elapsed_time(ev[2]))
+            if moe.moe_get_device_error() != 0:
+                raise SystemExit("device error in sweep")
+            g1, g2 = statistics.fmean(t1), statistics.fmean(t2)
+            n_live_exp = int((np.diff(off_np) > 0).sum())
+            flop = 2.0 * live * (2 * I * H + H * I)
+            wbytes = n_live_exp * (2 * I * H + H * I) * 2
+            abytes = live * (H + 2 * I) * 2 + M * H * 2
+            rows.append({"live": live, "layout": layout, "experts_live": n_live_exp, "gate_up_ms": g1,
+                         "down_ms": g2, "pair_ms": g1 + g2, "pair_tflops": flop / ((g1 + g2) * 1e-3) / 1e12,
+                         "pair_hbm_gbs": (wbytes + abytes) / ((g1 + g2) * 1e-3) / 1e9,
+                         "hbm_roofline_ms": (wbytes + abytes) / (pk["hbm_gbs"] * 1e9) * 1e3,
+                         "tensor_roofline_ms": flop / (pk["bf16_tflops"] * 1e12) * 1e3})
+    full = {r["layout"]: r["pair_ms"] for r in rows if r["live"] == 16384}
+    for r in rows:
+        r["time_vs_full"] = r["pair_ms"] / full[r["layout"]]
+    print(json.dumps({"metric": "grouped GEMM pair time vs live rows (sentinel sweep)", "unit": "ms",
+                      "config": {"workload": "sweep-128e-h2048-i768-m16384", "dtype": "bf16",
+                                 "l2": "flushed between steps", "steps": args.steps},
+                      "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"], "kind": pk_kind},
+                      "rows": rows}))
+    return 0
+
+
 # ------------------------------------------------------------------ main
 def main():
     args = parse()
     from grouped_gemm_serving_gb300 import synth
+    if args.workload == "sweep":
+        import torch
+        from grouped_gemm_serving_gb300 import build as gbuild
+        gbuild.build()
+        from grouped_gemm_serving_gb300 import moe
+        return sweep_main(args, synth, torch, moe)
     if args.workload in synth.WORKLOADS:
         wl = synth.WORKLOADS[args.workload]
     else:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(synth.WORKLOADS)}")
+    if args.experts:
+        wl = wl.with_(name=f"{wl.name}-scaled-e{args.experts}", E=args.experts,
+                      T=max(1, wl.T * args.experts // wl.E))
     if args.impl == "reference":
         return reference_main(args, wl, synth)
 
@@ -341,6 +428,13 @@ def main():
     torch.cuda.synchronize()
     step_ms = []
     with ClockSampler(local) as clk:
+        # untimed pre-roll (about 1 s) so that the 200 ms clock samples cover
+        # the GPU under this load, then the timed steps
+        t_pre = time.perf_counter()
+        while time.perf_counter() - t_pre < 1.0:
+            step.run()
+            torch.cuda.synchronize()
+        barrier()
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)

@@ -76,3 +76,28 @@ moe_status_t moe_get_device_error(int32_t* code, moe_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that
+// nothing ever arrives on, with the given limit, and records a timeout.
+namespace {
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    moe::mbar_init(moe::smem_u32(&bar), 1);
+    moe::fence_barrier_init();
+    if (!moe::mbar_wait(moe::smem_u32(&bar), 0, &abort_flag, limit_ns))
+        moe::raise_device_error(err, MOE_DEVERR_TIMEOUT);
+}
+}  // namespace
+
+extern "C" moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}

@@ -11,14 +11,15 @@
 // over rows sorted by expert id (grouped_mm backend, "Mixture of Experts in
 // transformers").
 //
-// Design (one persistent CTA per SM, 320 threads):
+// Design (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: A tile [128 rows x 128 bytes] and B tile
 //               [256 rows x 128 bytes] per k-block into a 4-stage ring;
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32 bytes) per
 //               k-block into one of two 256-column TMEM accumulators;
-//   warps 2-9   epilogue: tcgen05.ld the accumulator, apply the epilogue and
+//   warps 2-3   idle (they complete warpgroup 0 for the register split)
+//   warps 4-11  epilogue: tcgen05.ld the accumulator, apply the epilogue and
 //               store; warp w reads TMEM lanes 32*(w%4).., columns half
-//               (w-2)/4; then zero the sentinel rows [offsets[E], M_cap).
+//               (w-4)/4; then zero the sentinel rows [offsets[E], M_cap).
 // The tile list is built on the device from offsets: expert e owns
 // ceil(cnt_e/128) row tiles times n_tiles column tiles, ordered expert-major,
 // then column tile, then row tile, so CTAs that run at the same time share a
@@ -47,7 +48,7 @@ constexpr int BN = 256;
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kThreads = 128 + kEpiThreads;  // warpgroup 0: TMA, MMA, 2 idle warps
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kStageA = BM * 128;
 constexpr int kStageB = BN * 128;
@@ -55,6 +56,9 @@ constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kMaxE = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
+constexpr int kRegsLow = 56, kRegsHigh = 224;
+static_assert(128 * kRegsLow + kEpiThreads * kRegsHigh <= kThreads * 168,
+              "register split exceeds the launch allocation");
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
 
@@ -231,7 +235,7 @@ template <bool FP8, int EPI>
 __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;               // TMEM lane quarter this warp may access
-    const int hsel = (warp - 2) >> 2;     // which half of the tile's columns
+    const int hsel = (warp - 4) >> 2;     // which half of the tile's columns
     const int r = q * 32 + lane;          // accumulator row of this thread
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int acc = 0, xsel = 0;
@@ -281,21 +285,45 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
             const int nb0 = EPI == EPI_STORE ? (ti.col0 + hsel * 128) / 128 : ti.col0 / 128;
             const int nb1 = EPI == EPI_STORE ? nb0 : (p.half + ti.col0) / 128;
             const bool nb_ok = nb0 < p.nb_scale;
+            const bool row_ok = row < p.M_cap;
+            // scales of k-block kb are loaded two k-blocks ahead, so their
+            // global-load latency overlaps the promotion of earlier blocks
+            float pa[2], pb0[2], pb1[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const bool in = i < KB;
+                pa[i] = in && row_ok ? __ldg(p.a_scales + static_cast<int64_t>(i) * p.M_cap + row) : 0.0f;
+                pb0[i] = in && nb_ok ? __ldg(sb_row + nb0 * KB + i) : 0.0f;
+                pb1[i] = in && EPI != EPI_STORE ? __ldg(sb_row + nb1 * KB + i) : 0.0f;
+            }
             for (int kb = 0; kb < KB; ++kb) {
-                const float sa = row < p.M_cap ? __ldg(p.a_scales + static_cast<int64_t>(kb) * p.M_cap + row) : 0.0f;
-                const float s0 = nb_ok ? sa * __ldg(sb_row + nb0 * KB + kb) : 0.0f;
-                const float s1 = EPI == EPI_STORE ? s0 : sa * __ldg(sb_row + nb1 * KB + kb);
+                const float s0 = pa[0] * pb0[0];
+                const float s1 = EPI == EPI_STORE ? s0 : pa[0] * pb1[0];
+                pa[0] = pa[1];
+                pb0[0] = pb0[1];
+                pb1[0] = pb1[1];
+                const int kn = kb + 2;
+                if (kn < KB) {
+                    pa[1] = row_ok ? __ldg(p.a_scales + static_cast<int64_t>(kn) * p.M_cap + row) : 0.0f;
+                    pb0[1] = nb_ok ? __ldg(sb_row + nb0 * KB + kn) : 0.0f;
+                    if (EPI != EPI_STORE) pb1[1] = __ldg(sb_row + nb1 * KB + kn);
+                }
                 if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
                 moe::tc_fence_after();
                 const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
+                // two 32-column loads per wait
                 if (EPI == EPI_STORE) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
-                        moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t v0[32], v1[32];
+                        moe::tmem_ld32(ta + hsel * 128 + c * 64, v0);
+                        moe::tmem_ld32(ta + hsel * 128 + c * 64 + 32, v1);
                         moe::tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) a[c * 32 + i] = fmaf(s0, __uint_as_float(v[i]), a[c * 32 + i]);
+                        for (int i = 0; i < 32; ++i) {
+                            a[c * 64 + i] = fmaf(s0, __uint_as_float(v0[i]), a[c * 64 + i]);
+                            a[c * 64 + 32 + i] = fmaf(s0, __uint_as_float(v1[i]), a[c * 64 + 32 + i]);
+                        }
                     }
                 } else {
 #pragma unroll
@@ -371,7 +399,7 @@ __device__ void zero_sentinel_rows(const Params& p) {
     const int L = p.offsets[p.E];
     const int64_t rows = static_cast<int64_t>(p.M_cap) - L;
     if (rows <= 0) return;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kEpiThreads + (threadIdx.x - 64);
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kEpiThreads + (threadIdx.x - 128);
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * kEpiThreads;
     const int esz = EPI == EPI_SWIGLU_Q ? 1 : 2;
     const int64_t vpr = static_cast<int64_t>(p.out_cols) * esz / 16;
@@ -458,15 +486,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem = S.tmem_base;
     const int total = S.prefix[p.E] * p.n_tiles;
 
-    if (warp == 0) {
-        if (lane == 0) producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) mma_issuer<FP8>(stages, S, p, total, tmem);
-        __syncwarp();
-    } else {
+    // FP8 promotion keeps 128 fp32 accumulators per epilogue thread: move
+    // registers from warpgroup 0 (TMA, MMA) to the two epilogue warpgroups.
+    // 128 * kRegsLow + 256 * kRegsHigh = 384 * 168, the launch allocation.
+    if (warp >= 4) {
+        if (FP8) moe::reg_alloc<kRegsHigh>();
         epilogue<FP8, EPI>(S, p, total, tmem);
         zero_sentinel_rows<EPI>(p);
+    } else {
+        if (FP8) moe::reg_dealloc<kRegsLow>();
+        if (warp == 0) {
+            if (lane == 0) producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
+            __syncwarp();
+        } else if (warp == 1) {
+            if (lane == 0) mma_issuer<FP8>(stages, S, p, total, tmem);
+            __syncwarp();
+        }
     }
     moe::tc_fence_before();
     __syncthreads();

@@ -45,6 +45,7 @@ _SIGS = {
     "moe_abi_version": (C.c_int, []),
     "moe_status_string": (C.c_char_p, [_I]),
     "moe_get_device_error": (_S, [_P, _P]),
+    "moe_selftest_wait_timeout": (_S, [C.c_uint64, _P]),
     "moe_route_sort_workspace_size": (_Z, [_I, _I, _I]),
     "moe_route_sort": (_S, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_route_sort_noalloc": (_S, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -115,6 +116,10 @@ def moe_get_device_error(stream=None) -> int:
     if st not in (MOE_OK, MOE_ERR_DEVICE_CHECK, MOE_ERR_TIMEOUT):
         raise MoeError(st, "moe_get_device_error")
     return code.value
+
+
+def moe_selftest_wait_timeout(limit_ns: int, stream=None):
+    _check(lib().moe_selftest_wait_timeout(limit_ns, _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def moe_route_sort_workspace_size(T, E, k) -> int:

@@ -97,6 +97,16 @@ const char* moe_status_string(moe_status_t status);
 moe_status_t moe_get_device_error(int32_t* code /* host */, moe_stream_t stream);
 
 /*
+ * moe_selftest_wait_timeout: diagnostic of the failure path.  Launches one
+ * thread that waits on an mbarrier nothing ever arrives on, bounded by
+ * limit_ns (1 ns .. 2 s) exactly like the waits inside the GEMM pipeline; the
+ * wait gives up and records MOE_DEVERR_TIMEOUT in the device error word, and
+ * the context stays usable.  Returns MOE_ERR_INVALID_ARG for a limit outside
+ * the range.
+ */
+moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream);
+
+/*
  * moe_route_sort -- top-k routing, sentinel marking and the stable sort by
  * expert id ("MoE basics" and "pluggable expert backends" of "Mixture of
  * Experts in transformers"; section 2 of the transformers MoE/FP8 write-up).

@@ -89,3 +89,8 @@ def test_bf16_quantising_epilogue_is_unsupported(moe):
 def test_workspace_too_small_is_reported(moe):
     st = moe.lib().moe_route_sort(16, None, None, 16, 16, 64, 8, 2, 1, 16, 16, 16, 16, 4, None)
     assert st == moe.MOE_ERR_WORKSPACE
+
+
+def test_selftest_limit_is_checked_on_host(moe):
+    assert moe.lib().moe_selftest_wait_timeout(0, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.lib().moe_selftest_wait_timeout(3_000_000_000, None) == moe.MOE_ERR_INVALID_ARG

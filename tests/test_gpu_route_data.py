@@ -218,3 +218,13 @@ def test_invalid_offsets_are_rejected_on_device(moe):
     moe.moe_swiglu(y1, dev(off), 3, M_cap, I, h)
     assert moe.moe_get_device_error() == moe.MOE_DEVERR_OFFSETS
     assert np.all(host_bf16_bits(h).view(np.int16) == 3)     # nothing written
+
+
+def test_bounded_wait_times_out_and_context_survives(moe):
+    # a wait on an mbarrier nothing arrives on gives up after 20 ms and
+    # reports MOE_DEVERR_TIMEOUT; the next launches still work
+    moe.moe_selftest_wait_timeout(20_000_000)
+    assert moe.moe_get_device_error() == moe.MOE_DEVERR_TIMEOUT
+    assert moe.moe_get_device_error() == moe.MOE_DEVERR_NONE     # read-and-clear
+    r = moe.route_sort_t(8, 2, logits=torch.zeros((16, 8), device="cuda"))
+    assert np.array_equal(host(r["offsets"])[[0, -1]], [0, 32])
