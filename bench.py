@@ -104,6 +104,22 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ ranks
+def cross_rank_max(value: float, dist, device) -> float:
+    """The largest per-rank value (the slowest rank's time); identity on one rank."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of independent replicas: every rank's tokens over
+    the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------------ inputs
 def make_layer(wl, torch, moe, synth):
     """Seeded synthetic layer resident on the device (weights drawn on the host
@@ -447,10 +463,7 @@ def main():
     if moe.moe_get_device_error() != 0:
         raise SystemExit("device error in the timed region")
     ms = statistics.fmean(step_ms)
-    ms_t = torch.tensor([ms], device="cuda")
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = cross_rank_max(ms, dist, "cuda")
 
     # ---- e2e: moe_forward with host buffers (pinned), copies inside the timed region
     x_pin = torch.from_numpy(L["x_host"].view(np.int16)).pin_memory()
@@ -475,9 +488,7 @@ def main():
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     e2e_mean = statistics.fmean(e2e_ms)
-    e2e_t = torch.tensor([e2e_mean], device="cuda")
-    if dist is not None:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_max = cross_rank_max(e2e_mean, dist, "cuda")
     if moe.moe_get_device_error() != 0:
         raise SystemExit("device error in the e2e region")
 
@@ -507,7 +518,6 @@ def main():
     if os.path.exists(tp):
         with open(tp) as f:
             traffic = json.load(f).get("gemm_gate_up_swiglu_bytes")
-    tokens = wl.T * world
     cores, model = cpu_info()
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -519,7 +529,7 @@ def main():
                "host_cores": cores}
     clocks = clk.summary()
     line = {
-        "metric": METRIC, "value": tokens / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_tokens_per_s(wl.T, world, ms_max), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if wl.dtype == "fp8" else "bf16",
         "data": "synthetic (seeded numpy draws; random-init weights N(0,0.02))",
@@ -538,7 +548,7 @@ def main():
         "hbm": {"permute_gbs": fb["permute_bytes"] / (kt["permute"] * 1e-3) / 1e9,
                 "combine_gbs": fb["combine_bytes"] / (kt["combine"] * 1e-3) / 1e9,
                 "peak_gbs": pk["hbm_gbs"]},
-        "e2e": {"value": tokens / (float(e2e_t.item()) * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(wl.T, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2},
         "gpu_launches": step.launches_per_step() * args.steps,

@@ -108,3 +108,34 @@ def test_forward_host_io_equals_device_path(moe):
     assert np.array_equal(y_dev, y_host)
     y_again, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits)
     assert np.array_equal(y_dev, y_again)                     # bit-reproducible
+
+
+def test_expert_parallel_shards_on_one_gpu(moe):
+    """Expert parallelism ("Mixture of Experts in transformers"): two shards of
+    E/2 experts each, run one after the other through moe_forward with local
+    ids (picks of the other shard's experts become sentinels); their partial
+    outputs summed on the host equal the unsharded layer."""
+    wl = synth.Workload("ep-16e-top4", T=256, E=16, k=4, H=256, I=384, n_sentinel=20)
+    x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    logits, mask = synth.router_logits(wl), synth.sentinel_mask(wl)
+    ref = oracle.moe_forward(x, W1, W2, E=wl.E, k=wl.k, logits=logits, sentinel_mask=mask)
+    ids, w = ref["ids"], ref["w"]
+    total = np.zeros((wl.T, wl.H), np.float64)
+    E_loc = wl.E // 2
+    for r in range(2):
+        lo = r * E_loc
+        ids_loc = np.where((ids >= lo) & (ids < lo + E_loc), ids - lo, E_loc).astype(np.int32)
+        out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+        ids_d, w_d = dev(ids_loc), dev(w)
+        a = moe.forward_args(dtype=moe.MOE_BF16, T=wl.T, E=E_loc, k=wl.k, H=wl.H, I=wl.I, x=dev_bf16(x),
+                             W1=dev_bf16(W1[lo:lo + E_loc]), W2=dev_bf16(W2[lo:lo + E_loc]), out=out,
+                             topk_ids=ids_d, topk_w=w_d)
+        n = moe.moe_forward_workspace_size(a)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        moe.moe_forward(a, ws, n)
+        assert moe.moe_get_device_error() == 0
+        total += host_f32_from_bf16(out)
+    err = row_rel_err(total, ref["out"])
+    assert err.max() <= TOL["bf16"], err.max()
+    dead = (ids == wl.E).all(axis=1)
+    assert np.all(total[dead] == 0)
