@@ -54,6 +54,7 @@ constexpr int kStageA = BM * 128;
 constexpr int kStageB = BN * 128;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kMaxE = 256;
+constexpr int kScaleRing = 4;   // k-blocks of block-scale prefetch in the FP8 epilogue
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr int kRegsLow = 56, kRegsHigh = 224;
@@ -85,9 +86,11 @@ struct Shared {
     int valid;
     int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
     float amax_x[2][2][BM];
+    float scale_ring[kScaleRing * 3 * kEpiThreads];   // FP8 block scales in flight
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Shared);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct Tile {
     int e, row0, row_end, col0;
@@ -137,6 +140,35 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
     const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
         make_float2(__fdiv_rn(c, s), __fdiv_rn(d, s)), __NV_SATFINITE, __NV_E4M3);
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// FP8 promotion of one 64-column chunk of a k-block partial into the fp32
+// accumulators a[]: store layout -> a[c*64 .. c*64+63] += s0 * (x0 | x1);
+// SwiGLU layout -> gate a[c*32 ..] += s0 * x0 and up a[64 + c*32 ..] += s1 * x1.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, uint32_t v0, uint32_t v1) {
+    asm("{\n\t.reg .b64 acc, sv, vv;\n\t"
+        "mov.b64 acc, {%0, %1};\n\t"
+        "mov.b64 sv, {%2, %2};\n\t"
+        "mov.b64 vv, {%3, %4};\n\t"
+        "fma.rn.f32x2 acc, sv, vv, acc;\n\t"
+        "mov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s), "r"(v0), "r"(v1));
+}
+
+template <int EPI>
+__device__ __forceinline__ void promote_chunk(float (&a)[128], int c, float s0, float s1,
+                                              const uint32_t (&x0)[32], const uint32_t (&x1)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        if (EPI == EPI_STORE) {
+            ffma2(a[c * 64 + i], a[c * 64 + i + 1], s0, x0[i], x0[i + 1]);
+            ffma2(a[c * 64 + 32 + i], a[c * 64 + 33 + i], s0, x1[i], x1[i + 1]);
+        } else {
+            ffma2(a[c * 32 + i], a[c * 32 + i + 1], s0, x0[i], x0[i + 1]);
+            ffma2(a[64 + c * 32 + i], a[64 + c * 32 + i + 1], s1, x1[i], x1[i + 1]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- roles
@@ -286,64 +318,72 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
             const int nb1 = EPI == EPI_STORE ? nb0 : (p.half + ti.col0) / 128;
             const bool nb_ok = nb0 < p.nb_scale;
             const bool row_ok = row < p.M_cap;
-            // scales of k-block kb are loaded two k-blocks ahead, so their
-            // global-load latency overlaps the promotion of earlier blocks
-            float pa[2], pb0[2], pb1[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const bool in = i < KB;
-                pa[i] = in && row_ok ? __ldg(p.a_scales + static_cast<int64_t>(i) * p.M_cap + row) : 0.0f;
-                pb0[i] = in && nb_ok ? __ldg(sb_row + nb0 * KB + i) : 0.0f;
-                pb1[i] = in && EPI != EPI_STORE ? __ldg(sb_row + nb1 * KB + i) : 0.0f;
-            }
-            for (int kb = 0; kb < KB; ++kb) {
-                const float s0 = pa[0] * pb0[0];
-                const float s1 = EPI == EPI_STORE ? s0 : pa[0] * pb1[0];
-                pa[0] = pa[1];
-                pb0[0] = pb0[1];
-                pb1[0] = pb1[1];
-                const int kn = kb + 2;
-                if (kn < KB) {
-                    pa[1] = row_ok ? __ldg(p.a_scales + static_cast<int64_t>(kn) * p.M_cap + row) : 0.0f;
-                    pb0[1] = nb_ok ? __ldg(sb_row + nb0 * KB + kn) : 0.0f;
-                    if (EPI != EPI_STORE) pb1[1] = __ldg(sb_row + nb1 * KB + kn);
+            // Block scales travel through a per-thread ring of kScaleRing slots
+            // in shared memory, filled by 4-byte cp.async copies (one commit
+            // group per k-block) kScaleRing k-blocks before they are used, so
+            // their global-load latency stays off the promotion's critical path
+            // and they take no registers.  Layout [slot][value][thread] keeps
+            // the accesses free of bank conflicts.
+            constexpr int R = kScaleRing;
+            const int et = threadIdx.x - 128;                 // epilogue thread 0..255
+            float* ring = S.scale_ring;
+            auto prefetch = [&](int kq, int slot) {
+                if (kq < KB) {
+                    if (row_ok)
+                        moe::cp_async4(moe::smem_u32(ring + (slot * 3 + 0) * kEpiThreads + et),
+                                       p.a_scales + static_cast<int64_t>(kq) * p.M_cap + row);
+                    if (nb_ok)
+                        moe::cp_async4(moe::smem_u32(ring + (slot * 3 + 1) * kEpiThreads + et),
+                                       sb_row + nb0 * KB + kq);
+                    if (EPI != EPI_STORE)
+                        moe::cp_async4(moe::smem_u32(ring + (slot * 3 + 2) * kEpiThreads + et),
+                                       sb_row + nb1 * KB + kq);
                 }
+                moe::cp_async_commit();
+            };
+#pragma unroll
+            for (int i = 0; i < R; ++i) prefetch(i, i);
+            for (int kb = 0; kb < KB; ++kb) {
+                const int slot = kb % R;
+                moe::cp_async_wait<R - 1>();               // k-block kb's group has landed
+                const float sa = row_ok ? ring[(slot * 3 + 0) * kEpiThreads + et] : 0.0f;
+                const float sb0 = nb_ok ? ring[(slot * 3 + 1) * kEpiThreads + et] : 0.0f;
+                const float sb1 = EPI != EPI_STORE ? ring[(slot * 3 + 2) * kEpiThreads + et] : 0.0f;
+                const float s0 = sa * sb0;
+                const float s1 = EPI == EPI_STORE ? s0 : sa * sb1;
+                prefetch(kb + R, slot);
                 if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
                 moe::tc_fence_after();
                 const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
-                // two 32-column loads per wait
+                // Two chunks of 64 columns.  The TMEM buffer goes back to the
+                // MMA as soon as the second chunk is in registers, before its
+                // FMAs, to keep the promotion short on the MMA's critical path.
+                // Paired FMAs (fma.rn.f32x2) round each lane exactly as fmaf.
+                uint32_t x0[32], x1[32];
                 if (EPI == EPI_STORE) {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t v0[32], v1[32];
-                        moe::tmem_ld32(ta + hsel * 128 + c * 64, v0);
-                        moe::tmem_ld32(ta + hsel * 128 + c * 64 + 32, v1);
-                        moe::tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            a[c * 64 + i] = fmaf(s0, __uint_as_float(v0[i]), a[c * 64 + i]);
-                            a[c * 64 + 32 + i] = fmaf(s0, __uint_as_float(v1[i]), a[c * 64 + 32 + i]);
-                        }
-                    }
+                    moe::tmem_ld32(ta + hsel * 128, x0);
+                    moe::tmem_ld32(ta + hsel * 128 + 32, x1);
                 } else {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t g[32], u[32];
-                        moe::tmem_ld32(ta + hsel * 64 + c * 32, g);
-                        moe::tmem_ld32(ta + 128 + hsel * 64 + c * 32, u);
-                        moe::tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            a[c * 32 + i] = fmaf(s0, __uint_as_float(g[i]), a[c * 32 + i]);
-                            a[64 + c * 32 + i] = fmaf(s1, __uint_as_float(u[i]), a[64 + c * 32 + i]);
-                        }
-                    }
+                    moe::tmem_ld32(ta + hsel * 64, x0);
+                    moe::tmem_ld32(ta + 128 + hsel * 64, x1);
                 }
+                moe::tmem_ld_wait();
+                promote_chunk<EPI>(a, 0, s0, s1, x0, x1);
+                if (EPI == EPI_STORE) {
+                    moe::tmem_ld32(ta + hsel * 128 + 64, x0);
+                    moe::tmem_ld32(ta + hsel * 128 + 96, x1);
+                } else {
+                    moe::tmem_ld32(ta + hsel * 64 + 32, x0);
+                    moe::tmem_ld32(ta + 128 + hsel * 64 + 32, x1);
+                }
+                moe::tmem_ld_wait();
                 moe::tc_fence_before();
                 moe::mbar_arrive(bar(S.acc_empty[acc]));
                 acc ^= 1;
                 if (!acc) acc_phase ^= 1u;
+                promote_chunk<EPI>(a, 1, s0, s1, x0, x1);
             }
+            moe::cp_async_wait<0>();
             if (EPI == EPI_STORE) {
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.out_cols;
                 if (live) {

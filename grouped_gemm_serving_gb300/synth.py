@@ -77,6 +77,9 @@ WORKLOADS = {
     # 128-expert top-8, H=2048, I=768, Zipf(1.1) expert popularity
     "128e-top8-h2048-zipf": Workload("128e-top8-h2048-zipf", T=8192, E=128, k=8, H=2048,
                                      I=768, bias="zipf1.1"),
+    # decode-sized batch of the same 32-expert layer: 64 tokens
+    "32e-top4-h2880-t64": Workload("32e-top4-h2880-t64", T=64, E=32, k=4, H=2880, I=2880,
+                                   bias="normal0.5"),
     # 256-expert top-8 fine-grained FP8 layer, H=7168, I=2048
     "256e-top8-h7168-fp8": Workload("256e-top8-h7168-fp8", T=4096, E=256, k=8, H=7168,
                                     I=2048, dtype="fp8"),
