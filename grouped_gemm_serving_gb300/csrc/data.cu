@@ -44,7 +44,7 @@ permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, 
         }
         const uint4* src = x + static_cast<int64_t>(t) * row_vecs;
         uint4* dst = xp + static_cast<int64_t>(p) * row_vecs;
-#pragma unroll 4
+#pragma unroll 8
         for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
         if (x_scales)
             for (int g = lane; g < G; g += 32)
@@ -109,23 +109,37 @@ combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
         }
     }
     uint4* dst = out + static_cast<int64_t>(t) * row_vecs;
-    // the trip count is the same for every lane, so the shuffles see a full warp
+    // The trip counts are the same for every lane, so the shuffles see a full
+    // warp.  Up to eight slots' vectors are loaded before any is used, so they
+    // are in flight together; they are then accumulated in slot order.
+    constexpr int KG = 8;
     for (int c0 = 0; c0 < row_vecs; c0 += 32) {
         const int c = c0 + lane;
         const bool in_row = c < row_vecs;
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int row = __shfl_sync(0xffffffffu, my_row, j);
-            const float wj = __shfl_sync(0xffffffffu, my_w, j);
-            if (row < 0 || !in_row) continue;
-            const uint4 v = __ldg(Y2 + static_cast<int64_t>(row) * row_vecs + c);
-            const uint32_t vs[4] = {v.x, v.y, v.z, v.w};
+        for (int j0 = 0; j0 < k; j0 += KG) {
+            uint4 v[KG];
+            float wj[KG];
+            bool use[KG];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(wj, moe::bf16_lo(vs[i]), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(wj, moe::bf16_hi(vs[i]), acc[2 * i + 1]);
+            for (int g = 0; g < KG; ++g) {
+                const int j = j0 + g;
+                const int row = __shfl_sync(0xffffffffu, my_row, j & 31);
+                wj[g] = __shfl_sync(0xffffffffu, my_w, j & 31);
+                use[g] = j < k && row >= 0 && in_row;   // sentinel slots are skipped
+                v[g] = use[g] ? __ldg(Y2 + static_cast<int64_t>(row) * row_vecs + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+                if (!use[g]) continue;
+                const uint32_t vs[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(wj[g], moe::bf16_lo(vs[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wj[g], moe::bf16_hi(vs[i]), acc[2 * i + 1]);
+                }
             }
         }
         if (in_row)
