@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiler mode: W warm-up steps then K steps, nothing else (no clock "
+                         "pre-roll, end-to-end pass or CPU baseline), so launches can be counted")
     ap.add_argument("--experts", type=int, default=0,
                     help="shrink the workload to this many experts, tokens scaled alike "
                          "(same rows per expert; for small profiler captures)")
@@ -432,6 +435,14 @@ def main():
 
     L = make_layer(wl, torch, moe, synth)
     step = Step(wl, L, torch, moe)
+    if args.ncu:
+        for _ in range(args.warmup + args.steps):
+            step.run()
+        torch.cuda.synchronize()
+        err = moe.moe_get_device_error()
+        print(json.dumps({"mode": "ncu", "workload": wl.name, "launches_per_step": step.launches_per_step(),
+                          "steps": args.warmup + args.steps, "device_error": err}))
+        return 1 if err else 0
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     for i in range(max(3, args.warmup)):
         step.run()

@@ -59,6 +59,7 @@ __device__ __forceinline__ int checked_id(int id, int E, int* err) {
     return id;
 }
 
+template <int NV>   // logits per lane: E <= 32 * NV
 __global__ void __launch_bounds__(kThreads)
 route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias,
                 const uint8_t* __restrict__ mask, int32_t* ids, float* __restrict__ w, int T,
@@ -70,7 +71,6 @@ route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias
     int my_id = E;  // lane j < k: the id of slot j
 
     if (logits) {
-        constexpr int NV = kMaxE / 32;
         const float* row = logits + static_cast<int64_t>(t) * E;
         float v[NV];
 #pragma unroll
@@ -150,6 +150,21 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // warp w owns a contiguous run of at most 256 of the block's slots; its ids
+    // are loaded once, up front, so the loads overlap the count summation
+    const int64_t blk0 = static_cast<int64_t>(b) * slots_per_block;
+    const int64_t blk1 = blk0 + slots_per_block < R ? blk0 + slots_per_block : R;
+    const int per_warp = (slots_per_block + kWarps - 1) / kWarps;
+    const int64_t w0 = blk0 + static_cast<int64_t>(warp) * per_warp;
+    const int64_t w1 = w0 + per_warp < blk1 ? w0 + per_warp : blk1;
+    constexpr int kChunks = kMaxSlotsPerBlock / kWarps / 32;
+    int idr[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const int64_t sl = w0 + c * 32 + lane;
+        idr[c] = sl < w1 ? ids[sl] : 0;
+    }
+
     // 1. per bin: total over all blocks and the count in blocks before this one
     for (int bin = threadIdx.x; bin < nb; bin += kThreads) {
         int all = 0, before = 0;
@@ -195,17 +210,16 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
     }
     __syncthreads();
 
-    // 3. stable ranks: warp w owns a contiguous run of the block's slots
-    const int64_t blk0 = static_cast<int64_t>(b) * slots_per_block;
-    const int64_t blk1 = blk0 + slots_per_block < R ? blk0 + slots_per_block : R;
-    const int per_warp = (slots_per_block + kWarps - 1) / kWarps;
-    const int64_t w0 = blk0 + static_cast<int64_t>(warp) * per_warp;
-    const int64_t w1 = w0 + per_warp < blk1 ? w0 + per_warp : blk1;
+    // 3. stable ranks within the warp's run, in slot order
     const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c)
+        idr[c] = w0 + c * 32 + lane < w1 ? checked_id(idr[c], E, err) : -1;   // -1: no slot here
 
-    for (int64_t base = w0; base < w1; base += 32) {           // pass A: per-warp histogram
-        const int64_t s = base + lane;
-        const int id = s < w1 ? checked_id(ids[s], E, err) : -1;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {                         // pass A: per-warp histogram
+        if (w0 + c * 32 >= w1) break;
+        const int id = idr[c];
         const unsigned peers = __match_any_sync(0xffffffffu, id);
         if (id >= 0 && lane == __ffs(peers) - 1) whist[warp][id] += __popc(peers);
         __syncwarp();
@@ -220,9 +234,11 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
         }
     }
     __syncthreads();
-    for (int64_t base = w0; base < w1; base += 32) {           // pass B: positions
-        const int64_t s = base + lane;
-        const int id = s < w1 ? checked_id(ids[s], E, err) : -1;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {                         // pass B: positions
+        if (w0 + c * 32 >= w1) break;
+        const int64_t s = w0 + c * 32 + lane;
+        const int id = idr[c];
         const unsigned peers = __match_any_sync(0xffffffffu, id);
         int pos = 0;
         if (id >= 0) pos = start[id] + whist[warp][id] + __popc(peers & lt);
@@ -234,6 +250,20 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
         }
         __syncwarp();
     }
+}
+
+void launch_topk_hist(cudaStream_t s, const float* logits, const float* bias, const uint8_t* mask,
+                      int32_t* ids, float* w, int T, int E, int k, int renormalize,
+                      int slots_per_block, int* counts, int* err) {
+    const dim3 grid((T + kWarps - 1) / kWarps);
+    if (E <= 32)
+        route_topk_hist<1><<<grid, kThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, slots_per_block, counts, err);
+    else if (E <= 64)
+        route_topk_hist<2><<<grid, kThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, slots_per_block, counts, err);
+    else if (E <= 128)
+        route_topk_hist<4><<<grid, kThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, slots_per_block, counts, err);
+    else
+        route_topk_hist<8><<<grid, kThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, slots_per_block, counts, err);
 }
 
 }  // namespace
@@ -267,9 +297,8 @@ extern "C" moe_status_t moe_route_sort(const float* logits, const float* expert_
     const SortGeometry g = geometry(T, k);
     int* counts = static_cast<int*>(ws);
     MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(g.blocks) * (E + 1) * sizeof(int), s));
-    route_topk_hist<<<(T + kWarps - 1) / kWarps, kThreads, 0, s>>>(
-        logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
-        renormalize, g.slots_per_block, counts, err);
+    launch_topk_hist(s, logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E,
+                     k, renormalize, g.slots_per_block, counts, err);
     MOE_CHECK_LAUNCH();
     route_scatter<<<g.blocks, kThreads, 0, s>>>(topk_ids, static_cast<int64_t>(T) * k, E,
                                                 g.slots_per_block, g.blocks, counts, sorted_rows,
@@ -335,9 +364,8 @@ extern "C" moe_status_t moe_route_sort_noalloc(const float* logits, const float*
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, ints * sizeof(int), s));
-    route_topk_hist<<<(T + kWarps - 1) / kWarps, kThreads, 0, s>>>(
-        logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
-        renormalize, g.slots_per_block, counts, err);
+    launch_topk_hist(s, logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E,
+                     k, renormalize, g.slots_per_block, counts, err);
     MOE_CHECK_LAUNCH();
     route_scatter<<<g.blocks, kThreads, 0, s>>>(topk_ids, static_cast<int64_t>(T) * k, E,
                                                 g.slots_per_block, g.blocks, counts, sorted_rows,
