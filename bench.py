@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels one by one instead of replaying a CUDA graph")
     ap.add_argument("--ncu", action="store_true",
                     help="profiler mode: W warm-up steps then K steps, nothing else (no clock "
                          "pre-roll, end-to-end pass or CPU baseline), so launches can be counted")
@@ -449,6 +451,26 @@ def main():
     torch.cuda.synchronize()
     if moe.moe_get_device_error() != 0:
         raise SystemExit("device error during warm-up")
+    # The step's C-ABI calls are captured once into a CUDA graph and replayed,
+    # as a serving loop would, so that host launch gaps between its short
+    # kernels stay out of the step time.
+    run_step = step.run
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step.run()                        # one eager pass on the capture stream
+            with torch.cuda.graph(graph, stream=side):
+                step.run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        run_step = graph.replay
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize()
+        if moe.moe_get_device_error() != 0:
+            raise SystemExit("device error in the captured step")
 
     # ---- timed region: K steps, L2 flushed between steps (untimed)
     barrier()
@@ -459,16 +481,26 @@ def main():
         # the GPU under this load, then the timed steps
         t_pre = time.perf_counter()
         while time.perf_counter() - t_pre < 1.0:
-            step.run()
+            run_step()
             torch.cuda.synchronize()
         barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            s0.record()
+            run_step()
+            s1.record()
+            torch.cuda.synchronize()
+            step_ms.append(s0.elapsed_time(s1))
+        wall = time.perf_counter() - wall0
+        # per-kernel durations: K more steps launched eagerly with CUDA events
+        # between the kernels on the launching stream
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             step.run(record=True)
             torch.cuda.synchronize()
-            step_ms.append(step.collect())
-        wall = time.perf_counter() - wall0
+            step.collect()
     torch.cuda.synchronize()
     barrier()
     if moe.moe_get_device_error() != 0:
@@ -547,7 +579,8 @@ def main():
         "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I,
                    "bias": wl.bias, "live_rows": live, "experts_with_rows": experts_live,
                    "parallelism": f"replicas x{world} (no collective)",
-                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+                   "l2": "flushed between timed steps (256 MiB write, untimed)",
+                   "launch": "eager C-ABI calls" if args.no_graph else "CUDA graph of the step's C-ABI calls"},
         "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate_up + fused SwiGLU",
                      "achieved": ach1, "peak": peak, "unit": "TFLOP/s", "frac": ach1 / peak,
                      "peak_source": peak_note, "traffic": traffic,
