@@ -595,7 +595,7 @@ def main():
         "e2e": {"value": job_tokens_per_s(wl.T, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2},
-        "gpu_launches": step.launches_per_step() * args.steps,
+        "gpu_launches": step.launches_per_step() * args.steps * 2,   # graph replays + eager steps
         "clocks": clocks,
         "cpu_baseline": cpu,
         "wall_s_timed": wall,
