@@ -3,8 +3,9 @@
 One step = one pass of the whole hot path over one batch: route + sort,
 permute, grouped GEMM gate_up with fused SwiGLU, grouped GEMM down, weighted
 combine (FP8 workloads add the activation quantiser and use the quantising
-epilogue).  Default workload: the 32-expert top-4 layer (T=4096, H=I=2880,
-bf16, biased routing).  Prints one JSON line.
+epilogue).  --gather folds the permute into the gate_up GEMM.  Default
+workload: the 32-expert top-4 layer (T=4096, H=I=2880, bf16, biased routing).
+Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -42,6 +43,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of replaying a CUDA graph")
+    ap.add_argument("--gather", action="store_true",
+                    help="gather the gate_up GEMM's rows from token order inside the GEMM "
+                         "(moe_forward's MOE_FWD_GATHER) instead of a separate permute")
     ap.add_argument("--ncu", action="store_true",
                     help="profiler mode: W warm-up steps then K steps, nothing else (no clock "
                          "pre-roll, end-to-end pass or CPU baseline), so launches can be counted")
@@ -166,8 +170,9 @@ class Step:
     """The hot path as the chain of C-ABI calls moe_forward enqueues, with
     CUDA events between kernels on the launching stream."""
 
-    def __init__(self, wl, L, torch, moe):
+    def __init__(self, wl, L, torch, moe, separate_scatter=True):
         self.wl, self.L, self.torch, self.moe = wl, L, torch, moe
+        self.scatter = separate_scatter
         T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
         R = T * k
         self.fp8 = wl.dtype == "fp8"
@@ -179,14 +184,17 @@ class Step:
         self.rws = z(max(self.rws_bytes, 16))
         if self.fp8:
             self.xq, self.xs = z(T, H), z(T, H // 128, dt=torch.float32)
-            self.xp, self.xps = z(R, H), z(H // 128, R, dt=torch.float32)
+            if self.scatter:
+                self.xp, self.xps = z(R, H), z(H // 128, R, dt=torch.float32)
             self.h, self.hs = z(R, I), z(I // 128, R, dt=torch.float32)
         else:
-            self.xp, self.h = z(R, H, dt=torch.bfloat16), z(R, I, dt=torch.bfloat16)
+            if self.scatter:
+                self.xp = z(R, H, dt=torch.bfloat16)
+            self.h = z(R, I, dt=torch.bfloat16)
         self.y2 = z(R, H, dt=torch.bfloat16)
         self.out = z(T, H, dt=torch.bfloat16)
         self.names = (["route_sort"] + (["act_quant"] if self.fp8 else []) +
-                      ["permute", "gemm_gate_up_swiglu", "gemm_down", "combine"])
+                      (["permute"] if self.scatter else []) + ["gemm_gate_up_swiglu", "gemm_down", "combine"])
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(self.names) + 1)]
         self.times = {n: [] for n in self.names}
 
@@ -206,19 +214,28 @@ class Step:
         if self.fp8:
             moe.moe_act_quant_fp8(L["x"], T, H, self.xq, self.xs)
             mark()
-            moe.moe_permute(moe.MOE_FP8_E4M3_B128, self.xq, self.xs, T, H, k, self.sr, self.off, E, R,
-                            self.xp, self.xps)
-            mark()
-            moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, self.xp, self.xps, L["w1"], L["w1_s"], self.off, E, R,
-                                 2 * I, H, moe.MOE_EPI_SWIGLU_QUANT_FP8, self.h, self.hs)
+            if self.scatter:
+                moe.moe_permute(moe.MOE_FP8_E4M3_B128, self.xq, self.xs, T, H, k, self.sr, self.off, E, R,
+                                self.xp, self.xps)
+                mark()
+                moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, self.xp, self.xps, L["w1"], L["w1_s"], self.off, E,
+                                     R, 2 * I, H, moe.MOE_EPI_SWIGLU_QUANT_FP8, self.h, self.hs)
+            else:
+                moe.moe_grouped_gemm_gather(moe.MOE_FP8_E4M3_B128, self.xq, self.xs, T, k, self.sr, L["w1"],
+                                            L["w1_s"], self.off, E, R, 2 * I, H, moe.MOE_EPI_SWIGLU_QUANT_FP8,
+                                            self.h, self.hs)
             mark()
             moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, self.h, self.hs, L["w2"], L["w2_s"], self.off, E, R,
                                  H, I, moe.MOE_EPI_STORE, self.y2, None)
         else:
-            moe.moe_permute(moe.MOE_BF16, L["x"], None, T, H, k, self.sr, self.off, E, R, self.xp, None)
-            mark()
-            moe.moe_grouped_gemm(moe.MOE_BF16, self.xp, None, L["w1"], None, self.off, E, R, 2 * I, H,
-                                 moe.MOE_EPI_SWIGLU, self.h, None)
+            if self.scatter:
+                moe.moe_permute(moe.MOE_BF16, L["x"], None, T, H, k, self.sr, self.off, E, R, self.xp, None)
+                mark()
+                moe.moe_grouped_gemm(moe.MOE_BF16, self.xp, None, L["w1"], None, self.off, E, R, 2 * I, H,
+                                     moe.MOE_EPI_SWIGLU, self.h, None)
+            else:
+                moe.moe_grouped_gemm_gather(moe.MOE_BF16, L["x"], None, T, k, self.sr, L["w1"], None, self.off,
+                                            E, R, 2 * I, H, moe.MOE_EPI_SWIGLU, self.h, None)
             mark()
             moe.moe_grouped_gemm(moe.MOE_BF16, self.h, None, L["w2"], None, self.off, E, R, H, I,
                                  moe.MOE_EPI_STORE, self.y2, None)
@@ -232,16 +249,17 @@ class Step:
         return self.ev[0].elapsed_time(self.ev[-1])
 
 
-def flops_bytes(wl, live_rows, experts_live):
+def flops_bytes(wl, live_rows, experts_live, separate_scatter=False):
     """Algorithmic work of one step: GEMM FLOPs on live rows and the minimum
-    HBM bytes of each kernel (weights of experts with rows, activations once)."""
+    HBM bytes of each kernel (weights of experts with rows, activations once).
+    The gathered gate_up GEMM reads x itself: each token row once at least."""
     T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
     R = T * k
     wb = 1 if wl.dtype == "fp8" else 2
     ab = 1 if wl.dtype == "fp8" else 2
     f1 = 2.0 * live_rows * (2 * I) * H
     f2 = 2.0 * live_rows * H * I
-    b1 = experts_live * 2 * I * H * wb + live_rows * H * ab + live_rows * I * ab
+    b1 = experts_live * 2 * I * H * wb + (live_rows if separate_scatter else T) * H * ab + live_rows * I * ab
     b2 = experts_live * H * I * wb + live_rows * I * ab + R * H * 2
     bp = T * H * ab + live_rows * H * ab
     bc = live_rows * H * 2 + R * 12 + T * H * 2
@@ -436,7 +454,8 @@ def main():
             dist.barrier()
 
     L = make_layer(wl, torch, moe, synth)
-    step = Step(wl, L, torch, moe)
+    separate = not (args.gather and (wl.H * (1 if wl.dtype == "fp8" else 2)) % 128 == 0)
+    step = Step(wl, L, torch, moe, separate_scatter=separate)
     if args.ncu:
         for _ in range(args.warmup + args.steps):
             step.run()
@@ -515,7 +534,7 @@ def main():
     fa = moe.forward_args(dtype=moe.MOE_FP8_E4M3_B128 if wl.dtype == "fp8" else moe.MOE_BF16, T=wl.T, E=wl.E,
                           k=wl.k, H=wl.H, I=wl.I, x=x_pin, W1=L["w1"], W2=L["w2"], W1_scales=L.get("w1_s"),
                           W2_scales=L.get("w2_s"), out=out_pin, logits=lg_pin, expert_bias=L["bias"],
-                          renormalize=wl.renormalize, host_io=True)
+                          renormalize=wl.renormalize, host_io=True, gather=not separate)
     nws = moe.moe_forward_workspace_size(fa)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -543,7 +562,7 @@ def main():
     off = step.off.cpu().numpy()
     live = int(off[-1])
     experts_live = int((np.diff(off) > 0).sum())
-    fb = flops_bytes(wl, live, experts_live)
+    fb = flops_bytes(wl, live, experts_live, separate)
     kt = {n: statistics.fmean(v) for n, v in step.times.items()}
     pk, pk_kind = peaks()
     g1 = kt["gemm_gate_up_swiglu"]
@@ -560,7 +579,8 @@ def main():
     tp = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
     if os.path.exists(tp):
         with open(tp) as f:
-            traffic = json.load(f).get("gemm_gate_up_swiglu_bytes")
+            traffic = json.load(f).get("gemm_gate_up_swiglu_bytes" if separate
+                                       else "gemm_gate_up_swiglu_gather_bytes")
     cores, model = cpu_info()
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -579,9 +599,12 @@ def main():
         "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I,
                    "bias": wl.bias, "live_rows": live, "experts_with_rows": experts_live,
                    "parallelism": f"replicas x{world} (no collective)",
+                   "scatter": "separate kernel" if separate else "gathered inside the gate_up GEMM",
                    "l2": "flushed between timed steps (256 MiB write, untimed)",
                    "launch": "eager C-ABI calls" if args.no_graph else "CUDA graph of the step's C-ABI calls"},
-        "roofline": {"bound": "tensor", "kernel": "grouped GEMM gate_up + fused SwiGLU",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("grouped GEMM gate_up + fused SwiGLU" if separate else
+                                "grouped GEMM gate_up, A gathered from token order, + fused SwiGLU"),
                      "achieved": ach1, "peak": peak, "unit": "TFLOP/s", "frac": ach1 / peak,
                      "peak_source": peak_note, "traffic": traffic,
                      "algorithmic_flop": fb["gemm1_flop"], "algorithmic_bytes": fb["gemm1_bytes"]},
@@ -589,7 +612,8 @@ def main():
                  "down_frac": ach2 / peak,
                  "pair_tflops": (fb["gemm1_flop"] + fb["gemm2_flop"]) / ((g1 + g2) * 1e-3) / 1e12},
         "kernels_ms": kt,
-        "hbm": {"permute_gbs": fb["permute_bytes"] / (kt["permute"] * 1e-3) / 1e9,
+        "hbm": {"permute_gbs": (fb["permute_bytes"] / (kt["permute"] * 1e-3) / 1e9 if "permute" in kt
+                                else None),
                 "combine_gbs": fb["combine_bytes"] / (kt["combine"] * 1e-3) / 1e9,
                 "peak_gbs": pk["hbm_gbs"]},
         "e2e": {"value": job_tokens_per_s(wl.T, world, e2e_max), "unit": "tokens/s",

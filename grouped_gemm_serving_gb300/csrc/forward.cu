@@ -2,8 +2,10 @@
 // the fused pipeline of "LlamaFactory Triton fused MoE kernel" (section 1):
 // route + sort -> [quantise x] -> scatter -> grouped GEMM gate_up with fused
 // silu(gate) * up [and fused FP8 quantisation of h] -> grouped GEMM down ->
-// weighted gather.  Offsets stay on the device; there is no host
-// synchronisation.
+// weighted gather.  With MOE_FWD_GATHER the scatter is folded into the
+// gate_up GEMM, which then reads its rows from token order
+// (moe_grouped_gemm_gather) and no permuted copy of x is held.  Offsets stay
+// on the device; there is no host synchronisation.
 #include "common.cuh"
 
 namespace {
@@ -44,9 +46,18 @@ bool valid_args(const moe_forward_args* a) {
     return true;
 }
 
+// Whether the scatter runs as its own kernel: unless MOE_FWD_GATHER asks
+// otherwise, and always when the gathering GEMM cannot take H (it fetches
+// rows in whole 128-byte k-blocks).
+bool separate_scatter(const moe_forward_args* a) {
+    const int esz = a->dtype == MOE_FP8_E4M3_B128 ? 1 : 2;
+    return !(a->flags & MOE_FWD_GATHER) || (a->H * esz) % 128 != 0;
+}
+
 Layout layout(const moe_forward_args* a) {
     const size_t T = a->T, E = a->E, k = a->k, H = a->H, I = a->I, R = T * k;
     const bool fp8 = a->dtype == MOE_FP8_E4M3_B128;
+    const bool scatter = separate_scatter(a);
     Carver c;
     Layout l{};
     l.route = c.take(moe_route_sort_workspace_size(a->T, a->E, a->k));
@@ -58,12 +69,14 @@ Layout layout(const moe_forward_args* a) {
     if (fp8) {
         l.xq = c.take(T * H);
         l.xs = c.take(T * (H / 128) * 4);
-        l.xp = c.take(R * H);
-        l.xps = c.take((H / 128) * R * 4);
+        if (scatter) {
+            l.xp = c.take(R * H);
+            l.xps = c.take((H / 128) * R * 4);
+        }
         l.h = c.take(R * I);
         l.hs = c.take((I / 128) * R * 4);
     } else {
-        l.xp = c.take(R * H * 2);
+        if (scatter) l.xp = c.take(R * H * 2);
         l.h = c.take(R * I * 2);
     }
     l.y2 = c.take(R * H * 2);
@@ -100,6 +113,7 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
     const int T = a->T, E = a->E, k = a->k, H = a->H, I = a->I, R = T * k;
     const bool fp8 = a->dtype == MOE_FP8_E4M3_B128;
     const bool host_io = (a->flags & MOE_FWD_HOST_IO) != 0;
+    const bool scatter = separate_scatter(a);
 
     const void* x = a->x;
     const float* logits = a->logits;
@@ -127,24 +141,34 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
                            moe_route_sort_workspace_size(T, E, k), stream));
     void* y2 = base + l.y2;
     if (!fp8) {
-        void* xp = base + l.xp;
         void* h = base + l.h;
-        MOE_TRY(moe_permute(MOE_BF16, x, nullptr, T, H, k, sorted_rows, offsets, E, R, xp, nullptr, stream));
-        MOE_TRY(moe_grouped_gemm(MOE_BF16, xp, nullptr, a->W1, nullptr, offsets, E, R, 2 * I, H,
-                                 MOE_EPI_SWIGLU, h, nullptr, stream));
+        if (scatter) {
+            void* xp = base + l.xp;
+            MOE_TRY(moe_permute(MOE_BF16, x, nullptr, T, H, k, sorted_rows, offsets, E, R, xp, nullptr, stream));
+            MOE_TRY(moe_grouped_gemm(MOE_BF16, xp, nullptr, a->W1, nullptr, offsets, E, R, 2 * I, H,
+                                     MOE_EPI_SWIGLU, h, nullptr, stream));
+        } else {
+            MOE_TRY(moe_grouped_gemm_gather(MOE_BF16, x, nullptr, T, k, sorted_rows, a->W1, nullptr, offsets, E,
+                                            R, 2 * I, H, MOE_EPI_SWIGLU, h, nullptr, stream));
+        }
         MOE_TRY(moe_grouped_gemm(MOE_BF16, h, nullptr, a->W2, nullptr, offsets, E, R, H, I,
                                  MOE_EPI_STORE, y2, nullptr, stream));
     } else {
         uint8_t* xq = base + l.xq;
         float* xs = reinterpret_cast<float*>(base + l.xs);
-        uint8_t* xp = base + l.xp;
-        float* xps = reinterpret_cast<float*>(base + l.xps);
         uint8_t* h = base + l.h;
         float* hs = reinterpret_cast<float*>(base + l.hs);
         MOE_TRY(moe_act_quant_fp8(x, T, H, xq, xs, stream));
-        MOE_TRY(moe_permute(MOE_FP8_E4M3_B128, xq, xs, T, H, k, sorted_rows, offsets, E, R, xp, xps, stream));
-        MOE_TRY(moe_grouped_gemm(MOE_FP8_E4M3_B128, xp, xps, a->W1, a->W1_scales, offsets, E, R, 2 * I, H,
-                                 MOE_EPI_SWIGLU_QUANT_FP8, h, hs, stream));
+        if (scatter) {
+            uint8_t* xp = base + l.xp;
+            float* xps = reinterpret_cast<float*>(base + l.xps);
+            MOE_TRY(moe_permute(MOE_FP8_E4M3_B128, xq, xs, T, H, k, sorted_rows, offsets, E, R, xp, xps, stream));
+            MOE_TRY(moe_grouped_gemm(MOE_FP8_E4M3_B128, xp, xps, a->W1, a->W1_scales, offsets, E, R, 2 * I, H,
+                                     MOE_EPI_SWIGLU_QUANT_FP8, h, hs, stream));
+        } else {
+            MOE_TRY(moe_grouped_gemm_gather(MOE_FP8_E4M3_B128, xq, xs, T, k, sorted_rows, a->W1, a->W1_scales,
+                                            offsets, E, R, 2 * I, H, MOE_EPI_SWIGLU_QUANT_FP8, h, hs, stream));
+        }
         MOE_TRY(moe_grouped_gemm(MOE_FP8_E4M3_B128, h, hs, a->W2, a->W2_scales, offsets, E, R, H, I,
                                  MOE_EPI_STORE, y2, nullptr, stream));
     }

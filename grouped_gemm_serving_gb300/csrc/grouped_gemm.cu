@@ -16,7 +16,8 @@
 //               [256 rows x 128 bytes] per k-block into a 4-stage ring;
 //   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32 bytes) per
 //               k-block into one of two 256-column TMEM accumulators;
-//   warps 2-3   idle (they complete warpgroup 0 for the register split)
+//   warps 2-3   idle (they complete warpgroup 0 for the register split),
+//               except with gathered A (below)
 //   warps 4-11  epilogue: tcgen05.ld the accumulator, apply the epilogue and
 //               store; warp w reads TMEM lanes 32*(w%4).., columns half
 //               (w-4)/4; then zero the sentinel rows [offsets[E], M_cap).
@@ -29,6 +30,18 @@
 // across tiles).  FP8: each 128-wide k-block is an exact e4m3 x e4m3 partial
 // in TMEM; the epilogue promotes it with sa[row, kb] * sb[block, kb] into fp32
 // registers while the MMA fills the other buffer.
+//
+// Gathered A (moe_grouped_gemm_gather): instead of one tile load from a
+// permuted buffer, the A tile is fetched four rows at a time with TMA
+// tile::gather4 loads straight from token order (row p = x[sorted_rows[p] /
+// k]), into the same 128-byte-swizzled layout and counted on the same stage
+// barrier as the weight tile; only the quads that hold live rows are fetched.
+// The gathers of a stage are shared by warps 0, 2 and 3 (one issuing lane
+// each).  This folds the scatter of "LlamaFactory Triton fused MoE kernel"
+// (section 1) into the first GEMM.  A gather4 costs far more than a quarter of
+// a 128-row tile load, and every A tile is fetched again for each column tile,
+// so this pays only when experts hold few rows (decode); with full tiles the
+// separate scatter is faster.
 //
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records
 // MOE_DEVERR_TIMEOUT, stops all roles, waits (bounded) for its in-flight TMA
@@ -55,17 +68,19 @@ constexpr int kStageB = BN * 128;
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kMaxE = 256;
 constexpr int kScaleRing = 4;   // k-blocks of block-scale prefetch in the FP8 epilogue
+constexpr int kGatherWarps = 3; // warps 0, 2, 3 issue the row gathers of gathered A
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr int kRegsLow = 56, kRegsHigh = 224;
 static_assert(128 * kRegsLow + kEpiThreads * kRegsHigh <= kThreads * 168,
               "register split exceeds the launch allocation");
+static_assert(kGatherWarps >= 1 && kGatherWarps <= 3, "gathering warps are 0, 2 and 3 of warpgroup 0");
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
 
 struct Params {
     const int32_t* offsets;
-    const float* a_scales;  // FP8: [K/128, M_cap]
+    const float* a_scales;  // FP8: [K/128, M_cap]; gathered: [T, K/128]
     const float* b_scales;  // FP8: [E, nb_scale, K/128]
     void* out;              // bf16 [M_cap, out_cols], or e4m3 for EPI_SWIGLU_Q
     float* out_scales;      // EPI_SWIGLU_Q: [out_cols/128, M_cap]
@@ -74,6 +89,10 @@ struct Params {
     int half;      // SwiGLU: N/2 (gate rows [0, half), up rows [half, N))
     int out_cols;  // N (store) or N/2 (SwiGLU)
     int n_tiles, k_blocks, nb_scale;
+    // gathered A (gx != nullptr): row p of A is row sorted_rows[p] / topk of gx
+    const uint8_t* gx;
+    const int32_t* sorted_rows;
+    int T, topk;
 };
 
 struct Shared {
@@ -85,6 +104,7 @@ struct Shared {
     int abort_flag;
     int valid;
     int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
+    alignas(16) int gtok[kGatherWarps][BM];  // gathered A: each issuing warp's copy of the tile's tokens
     float amax_x[2][2][BM];
     float scale_ring[kScaleRing * 3 * kEpiThreads];   // FP8 block scales in flight
 };
@@ -211,6 +231,105 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     }
 }
 
+// Source token of row `row` of the permuted order, or -1 when the row is past
+// the tile's expert or its slot is out of range (that case is reported).
+__device__ __forceinline__ int gather_token(const Params& p, int row, int row_end, bool report) {
+    if (row >= row_end) return -1;
+    const int slot = p.sorted_rows[row];
+    const int t = slot >= 0 ? slot / p.topk : -1;
+    if (t < 0 || t >= p.T) {
+        if (report) moe::raise_device_error(p.err, MOE_DEVERR_ROUTE);
+        return -1;
+    }
+    return t;
+}
+
+// Producer for gathered A, run by issuing warp g (0 = warp 0, which also
+// posts the stage's byte count and loads the weight tile).  The warp reads the
+// tile's 128 tokens; then its lane 0 waits for each stage and gathers rows
+// 4j..4j+3 for j = g, g + kGatherWarps, ... below the tile's live rows.
+// Gathered bytes may land before warp 0 posts the count: the barrier's
+// transaction count goes negative until then, and the phase cannot complete
+// before warp 0's arrival.  A row without a token inside a fetched quad (past
+// the expert's end, or an out-of-range slot) is fetched from token 0, so every
+// coordinate stays inside the tensor; the epilogue never stores such a row.
+template <bool FP8, int EPI>
+__device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* stages,
+                                Shared& S, const Params& p, int total, int g) {
+    const int lane = threadIdx.x & 31;
+    int* gtok = S.gtok[g];
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const Tile ti = decode_tile(t, S, p);
+        __syncwarp();  // lane 0 is done with the previous tile's tokens
+#pragma unroll
+        for (int j = 0; j < BM / 32; ++j) {
+            const int tok = gather_token(p, ti.row0 + lane + 32 * j, ti.row_end, g == 0);
+            gtok[lane + 32 * j] = tok >= 0 ? tok : 0;
+        }
+        __syncwarp();
+        // only the quads that hold a live row are fetched; the rest of the A
+        // tile keeps stale bytes, which only feed rows the epilogue drops
+        const int nq = (min(BM, ti.row_end - ti.row0) + 3) / 4;
+        if (lane == 0) {
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar(S.full[stage]);
+                const uint32_t sa = moe::smem_u32(stages + stage * kStageBytes);
+                const int kc = kb * (FP8 ? 128 : 64);
+                if (g == 0) {
+                    moe::mbar_arrive_expect_tx(fb, kStageB + nq * 512);
+                    const uint32_t sb = sa + kStageA;
+                    if (EPI == EPI_STORE) {
+                        moe::tma_load_3d(sb, tmB, fb, kc, ti.col0, ti.e);
+                    } else {
+                        moe::tma_load_4d(sb, tmB, fb, kc, ti.col0, 0, ti.e);
+                        moe::tma_load_4d(sb + (BN / 2) * 128, tmB, fb, kc, ti.col0, 1, ti.e);
+                    }
+                }
+                // token quads are read four at a time before their gathers
+                // are issued, so the shared-memory loads overlap instead of
+                // each waiting behind the previous gather (16 registers)
+                constexpr int NQ = (BM / 4 + kGatherWarps - 1) / kGatherWarps, CH = 4;
+#pragma unroll
+                for (int c = 0; c < NQ; c += CH) {
+                    int4 r[CH];
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        const int j = g + (c + i) * kGatherWarps;
+                        r[i] = c + i < NQ && j < nq ? *reinterpret_cast<const int4*>(gtok + 4 * j)
+                                                    : make_int4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        const int j = g + (c + i) * kGatherWarps;
+                        if (c + i < NQ && j < nq)
+                            moe::tma_gather4(sa + j * 512, tmA, fb, kc, r[i].x, r[i].y, r[i].z, r[i].w);
+                    }
+                }
+                issued |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (!ok && lane == 0) {
+        fail(S, p);
+        // this warp's gathers land whatever the other roles do; the phases
+        // they count towards may never complete, so each wait is short
+        int zero = 0;
+        for (int s = 0; s < kStages; ++s)
+            if ((issued >> s) & 1u)
+                moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
+    }
+}
+
 template <bool FP8>
 __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int total, uint32_t tmem) {
     constexpr uint32_t idesc = moe::make_idesc(FP8 ? 0u : 1u, BM, BN);
@@ -317,7 +436,21 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
             const int nb0 = EPI == EPI_STORE ? (ti.col0 + hsel * 128) / 128 : ti.col0 / 128;
             const int nb1 = EPI == EPI_STORE ? nb0 : (p.half + ti.col0) / 128;
             const bool nb_ok = nb0 < p.nb_scale;
-            const bool row_ok = row < p.M_cap;
+            // activation scales of this row: group-major over permuted rows,
+            // or row-major over tokens when A is gathered
+            const float* sa_row;
+            int sa_step;
+            bool row_ok;
+            if (p.gx) {
+                const int tok = gather_token(p, row, ti.row_end, false);
+                row_ok = tok >= 0;
+                sa_row = p.a_scales + static_cast<int64_t>(row_ok ? tok : 0) * KB;
+                sa_step = 1;
+            } else {
+                row_ok = row < p.M_cap;
+                sa_row = p.a_scales + row;
+                sa_step = p.M_cap;
+            }
             // Block scales travel through a per-thread ring of kScaleRing slots
             // in shared memory, filled by 4-byte cp.async copies (one commit
             // group per k-block) kScaleRing k-blocks before they are used, so
@@ -331,7 +464,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
                 if (kq < KB) {
                     if (row_ok)
                         moe::cp_async4(moe::smem_u32(ring + (slot * 3 + 0) * kEpiThreads + et),
-                                       p.a_scales + static_cast<int64_t>(kq) * p.M_cap + row);
+                                       sa_row + static_cast<int64_t>(kq) * sa_step);
                     if (nb_ok)
                         moe::cp_async4(moe::smem_u32(ring + (slot * 3 + 1) * kEpiThreads + et),
                                        sb_row + nb0 * KB + kq);
@@ -492,6 +625,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
         }
         if (lane == 0 && (p.offsets[0] != 0 || p.offsets[p.E] > p.M_cap)) bad = 1;
+        // gathered A: sorted_rows holds T * topk entries
+        if (lane == 0 && p.gx && p.offsets[p.E] > p.T * p.topk) bad = 1;
         bad = __any_sync(0xffffffffu, bad);
         int incl = sum;
 #pragma unroll
@@ -535,7 +670,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         zero_sentinel_rows<EPI>(p);
     } else {
         if (FP8) moe::reg_dealloc<kRegsLow>();
-        if (warp == 0) {
+        if (p.gx && (warp == 0 || warp - 1 < kGatherWarps) && warp != 1) {
+            producer_gather<FP8, EPI>(&tmA, &tmB, stages, S, p, total, warp == 0 ? 0 : warp - 1);
+            __syncwarp();
+        } else if (warp == 0) {
             if (lane == 0) producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
             __syncwarp();
         } else if (warp == 1) {
@@ -596,12 +734,12 @@ moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params
     return MOE_OK;
 }
 
-}  // namespace
-
-extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,
-                                         const void* B, const float* B_scales, const int32_t* offsets,
-                                         int E, int M_cap, int N, int K, moe_epilogue_t epilogue,
-                                         void* C, float* C_scales, moe_stream_t stream) {
+// Shared by both entry points.  With gx set, A is gathered from token order
+// (gx [T, K], sorted_rows [T*topk]) and the A tensor map is never used.
+moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales, const void* gx,
+                              const int32_t* sorted_rows, int T, int topk, const void* B,
+                              const float* B_scales, const int32_t* offsets, int E, int M_cap, int N, int K,
+                              moe_epilogue_t epilogue, void* C, float* C_scales, moe_stream_t stream) {
     MOE_CHECK_ARG(A && B && offsets && C && E >= 1 && E <= kMaxE && M_cap >= 1 && N >= 8 && K >= 8);
     MOE_CHECK_ARG(moe::aligned16(A) && moe::aligned16(B) && moe::aligned16(C));
     const bool fp8 = dtype == MOE_FP8_E4M3_B128;
@@ -618,6 +756,12 @@ extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const
     } else {
         MOE_CHECK_ARG(K % 8 == 0);
     }
+    const int esz = fp8 ? 1 : 2;
+    if (gx) {
+        MOE_CHECK_ARG(sorted_rows && T >= 1 && topk >= 1 && static_cast<int64_t>(T) * topk < INT_MAX);
+        // gathered rows are fetched in whole 128-byte k-blocks, never past the row
+        if ((static_cast<int64_t>(K) * esz) % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    }
     const int half = swiglu ? N / 2 : 0;
     const int n_tiles = swiglu ? (half + BN / 2 - 1) / (BN / 2) : (N + BN - 1) / BN;
     const int64_t max_tiles = (static_cast<int64_t>(M_cap) / BM + E) * n_tiles;
@@ -625,13 +769,13 @@ extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
 
-    const int esz = fp8 ? 1 : 2;
     const cuuint32_t bk = 128 / esz;  // elements in a 128-byte k-block row
     CUtensorMap tmA, tmB;
     {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M_cap)};
+        // permuted A: 128-row tiles; gathered A: x [T, K] read a row at a time
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(gx ? T : M_cap)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * esz};
-        const cuuint32_t box[2] = {bk, BM};
+        const cuuint32_t box[2] = {bk, gx ? 1u : static_cast<cuuint32_t>(BM)};
         if (!encode(&tmA, fp8, A, 2, dims, strides, box)) return MOE_ERR_CUDA;
     }
     if (!swiglu) {
@@ -665,6 +809,10 @@ extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const
     p.n_tiles = n_tiles;
     p.k_blocks = (K + static_cast<int>(bk) - 1) / static_cast<int>(bk);
     p.nb_scale = (N + 127) / 128;
+    p.gx = static_cast<const uint8_t*>(gx);
+    p.sorted_rows = sorted_rows;
+    p.T = gx ? T : 0;
+    p.topk = gx ? topk : 1;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fp8) {
         if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, p, s);
@@ -673,4 +821,24 @@ extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const
     }
     if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE>(tmA, tmB, p, s);
     return launch<false, EPI_SWIGLU>(tmA, tmB, p, s);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,
+                                         const void* B, const float* B_scales, const int32_t* offsets,
+                                         int E, int M_cap, int N, int K, moe_epilogue_t epilogue,
+                                         void* C, float* C_scales, moe_stream_t stream) {
+    return run_grouped_gemm(dtype, A, A_scales, nullptr, nullptr, 0, 0, B, B_scales, offsets, E, M_cap, N, K,
+                            epilogue, C, C_scales, stream);
+}
+
+extern "C" moe_status_t moe_grouped_gemm_gather(moe_dtype_t dtype, const void* x, const float* x_scales, int T,
+                                                int k, const int32_t* sorted_rows, const void* B,
+                                                const float* B_scales, const int32_t* offsets, int E, int M_cap,
+                                                int N, int K, moe_epilogue_t epilogue, void* C, float* C_scales,
+                                                moe_stream_t stream) {
+    MOE_CHECK_ARG(x && sorted_rows);
+    return run_grouped_gemm(dtype, x, x_scales, x, sorted_rows, T, k, B, B_scales, offsets, E, M_cap, N, K,
+                            epilogue, C, C_scales, stream);
 }

@@ -22,6 +22,7 @@ MOE_BF16, MOE_FP8_E4M3_B128 = 0, 1
 MOE_EPI_STORE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_QUANT_FP8 = 0, 1, 2
 MOE_DEVERR_NONE, MOE_DEVERR_OFFSETS, MOE_DEVERR_TIMEOUT, MOE_DEVERR_ROUTE = 0, 1, 2, 3
 MOE_FWD_HOST_IO = 1
+MOE_FWD_GATHER = 2
 
 
 class MoeError(RuntimeError):
@@ -53,6 +54,7 @@ _SIGS = {
     "moe_weight_quant_fp8": (_S, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_S, [_I, _P, _P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm": (_S, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_grouped_gemm_gather": (_S, [_I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_swiglu": (_S, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_combine": (_S, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_forward_workspace_size": (_Z, [C.POINTER(ForwardArgs)]),
@@ -164,6 +166,14 @@ def moe_grouped_gemm(dtype, A, A_scales, B, B_scales, offsets, E, M_cap, N, K, e
            "moe_grouped_gemm")
 
 
+def moe_grouped_gemm_gather(dtype, x, x_scales, T, k, sorted_rows, B, B_scales, offsets, E, M_cap, N, K,
+                            epilogue, Cout, C_scales, stream=None):
+    _check(lib().moe_grouped_gemm_gather(dtype, _p(x), _p(x_scales), T, k, _p(sorted_rows), _p(B), _p(B_scales),
+                                         _p(offsets), E, M_cap, N, K, epilogue, _p(Cout), _p(C_scales),
+                                         _stream(stream)),
+           "moe_grouped_gemm_gather")
+
+
 def moe_swiglu(Y1, offsets, E, M_cap, I, h, stream=None):
     _check(lib().moe_swiglu(_p(Y1), _p(offsets), E, M_cap, I, _p(h), _stream(stream)), "moe_swiglu")
 
@@ -206,15 +216,16 @@ def route_sort_t(E: int, k: int, *, logits=None, expert_bias=None, sentinel_mask
 
 def forward_args(*, dtype, T, E, k, H, I, x, W1, W2, out, logits=None, expert_bias=None,
                  sentinel_mask=None, topk_ids=None, topk_w=None, W1_scales=None, W2_scales=None,
-                 renormalize=True, host_io=False) -> ForwardArgs:
-    """Fill a ForwardArgs from tensors (or raw addresses).  The returned
-    struct keeps the given tensors alive for as long as it lives."""
+                 renormalize=True, host_io=False, gather=False) -> ForwardArgs:
+    """Fill a ForwardArgs from tensors (or raw addresses); ``gather`` sets
+    MOE_FWD_GATHER.  The returned struct keeps the given tensors alive for as
+    long as it lives."""
     a = ForwardArgs()
     a._keepalive = [logits, expert_bias, sentinel_mask, topk_ids, topk_w, x, W1, W1_scales, W2,
                     W2_scales, out]
     a.dtype, a.T, a.E, a.k, a.H, a.I = dtype, T, E, k, H, I
     a.renormalize = int(renormalize)
-    a.flags = MOE_FWD_HOST_IO if host_io else 0
+    a.flags = (MOE_FWD_HOST_IO if host_io else 0) | (MOE_FWD_GATHER if gather else 0)
     a.logits, a.expert_bias, a.sentinel_mask = _p(logits), _p(expert_bias), _p(sentinel_mask)
     a.topk_ids, a.topk_w = _p(topk_ids), _p(topk_w)
     a.x, a.W1, a.W1_scales, a.W2, a.W2_scales, a.out = (_p(x), _p(W1), _p(W1_scales), _p(W2),

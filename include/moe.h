@@ -233,6 +233,31 @@ moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
                               float* C_scales, moe_stream_t stream);
 
 /*
+ * moe_grouped_gemm_gather -- moe_grouped_gemm with the scatter of the
+ * LlamaFactory write-up (section 1) folded into the A operand: row p of A is
+ * x[sorted_rows[p] / k], read straight from token order, so no permuted copy
+ * of the activations is written.  Same arithmetic, tile order and results as
+ * moe_permute followed by moe_grouped_gemm, bit for bit.
+ *
+ * x            bf16 [T, K], or e4m3 [T, K] with x_scales fp32 [T, K/128]
+ *              (row-major, as moe_act_quant_fp8 writes them)
+ * sorted_rows  int32 [T*k] as written by moe_route_sort (device)
+ * B, B_scales, offsets, E, M_cap, N, K, epilogue, C, C_scales: as in
+ *              moe_grouped_gemm (C has M_cap rows in permuted order).
+ * Limits: those of moe_grouped_gemm, plus K * element size a multiple of 128
+ *   bytes (MOE_ERR_UNSUPPORTED otherwise: rows are fetched in whole 128-byte
+ *   k-blocks), offsets[E] <= T*k (checked on the device: MOE_DEVERR_OFFSETS,
+ *   nothing is computed) and every sorted_rows[p], p < offsets[E], in [0, T*k)
+ *   (MOE_DEVERR_ROUTE; that row of C is not meaningful, the others are
+ *   unaffected).
+ */
+moe_status_t moe_grouped_gemm_gather(moe_dtype_t dtype, const void* x, const float* x_scales, int T,
+                                     int k, const int32_t* sorted_rows, const void* B,
+                                     const float* B_scales, const int32_t* offsets, int E,
+                                     int M_cap, int N, int K, moe_epilogue_t epilogue, void* C,
+                                     float* C_scales, moe_stream_t stream);
+
+/*
  * moe_swiglu -- standalone silu(gate) * up (LlamaFactory write-up, section
  * 1): h[p, n] = g / (1 + exp(-g)) * Y1[p, I + n] with g = Y1[p, n], for
  * p < offsets[E]; rows p >= offsets[E] of h are written as zeros.
@@ -260,13 +285,22 @@ moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* t
 #define MOE_FWD_HOST_IO 1u /* x, logits and out are HOST pointers (pinned memory
                               recommended); the call stages them through the
                               workspace with cudaMemcpyAsync on `stream` */
+#define MOE_FWD_GATHER 2u  /* fold the scatter into the gate_up GEMM
+                              (moe_grouped_gemm_gather instead of moe_permute
+                              + moe_grouped_gemm): same results, bit for bit,
+                              and no permuted copy of x (R*H*element-size
+                              bytes less workspace), but slower on GB300 (the
+                              GEMM fetches its rows four at a time, for every
+                              column tile).  Ignored when H * element size is
+                              not a multiple of 128. */
 
 /*
  * moe_forward -- the whole expert layer on one stream, in the order of the
  * LlamaFactory pipeline: route + sort, [quantise x], permute, grouped GEMM
  * gate_up with the SwiGLU (and, for FP8, the quantisation of h) fused into
  * its epilogue, grouped GEMM down (sentinel rows zero), weighted combine.
- * No host synchronisation; offsets never leave the device.
+ * With MOE_FWD_GATHER the permute is folded into the gate_up GEMM.  No host
+ * synchronisation; offsets never leave the device.
  */
 typedef struct {
     moe_dtype_t dtype;

@@ -48,7 +48,11 @@ def test_workspace_sizes(moe):
     a = moe.forward_args(dtype=moe.MOE_BF16, T=4096, E=32, k=4, H=2880, I=2880, x=1 << 20, W1=1 << 21,
                          W2=1 << 22, out=1 << 23, logits=1 << 24)
     R = 4096 * 4
-    assert moe.moe_forward_workspace_size(a) >= R * 2880 * 2 * 2 + R * 2880 * 2
+    fused = moe.moe_forward_workspace_size(a)
+    assert fused >= R * 2880 * 2 * 3                  # permuted x, h and the down output
+    gat = moe.forward_args(dtype=moe.MOE_BF16, T=4096, E=32, k=4, H=2880, I=2880, x=1 << 20, W1=1 << 21,
+                           W2=1 << 22, out=1 << 23, logits=1 << 24, gather=True)
+    assert moe.moe_forward_workspace_size(gat) == fused - R * 2880 * 2   # no permuted copy of x
     bad = moe.forward_args(dtype=moe.MOE_FP8_E4M3_B128, T=64, E=8, k=2, H=2880, I=2880, x=1 << 20,
                            W1=1 << 21, W2=1 << 22, out=1 << 23, logits=1 << 24)
     assert moe.moe_forward_workspace_size(bad) == 0   # FP8 needs multiples of 128 and scales
@@ -72,6 +76,12 @@ def test_workspace_sizes(moe):
     ("moe_grouped_gemm", (1, 16, 16, 16, 16, 16, 8, 64, 256, 100, 0, 16, None, None)),
     ("moe_grouped_gemm", (1, 16, 16, 16, 16, 16, 8, 64, 192, 128, 1, 16, None, None)),
     ("moe_grouped_gemm", (0, 16, None, 16, None, 16, 8, 64, 256, 64, 7, 16, None, None)),
+    # gathered A: no sorted_rows, no tokens, k = 0, x misaligned, FP8 K not a multiple of 128
+    ("moe_grouped_gemm_gather", (0, 16, None, 4, 2, None, 16, None, 16, 8, 64, 64, 64, 0, 16, None, None)),
+    ("moe_grouped_gemm_gather", (0, 16, None, 0, 2, 16, 16, None, 16, 8, 64, 64, 64, 0, 16, None, None)),
+    ("moe_grouped_gemm_gather", (0, 16, None, 4, 0, 16, 16, None, 16, 8, 64, 64, 64, 0, 16, None, None)),
+    ("moe_grouped_gemm_gather", (0, 18, None, 4, 2, 16, 16, None, 16, 8, 64, 64, 64, 0, 16, None, None)),
+    ("moe_grouped_gemm_gather", (1, 16, 16, 4, 2, 16, 16, 16, 16, 8, 64, 256, 100, 0, 16, None, None)),
     ("moe_swiglu", (16, 16, 8, 64, 12, 16, None)),
     ("moe_combine", (16, 16, 16, 16, 4, 2, 12, 8, 16, None)),
     ("moe_combine", (16, 16, 16, 16, 4, 40, 16, 64, 16, None)),
@@ -84,6 +94,24 @@ def test_host_side_argument_checks(moe, call):
 def test_bf16_quantising_epilogue_is_unsupported(moe):
     st = moe.lib().moe_grouped_gemm(0, 16, None, 16, None, 16, 8, 64, 256, 64, 2, 16, None, None)
     assert st == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_gather_needs_whole_128_byte_k_blocks(moe):
+    # bf16 K = 200 is 400 bytes per row: not a whole number of k-blocks
+    st = moe.lib().moe_grouped_gemm_gather(0, 16, None, 4, 2, 16, 16, None, 16, 8, 64, 64, 200, 0, 16, None, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_forward_gathers_only_whole_k_blocks(moe):
+    # H = 200 (bf16) cannot be gathered: the separate scatter's buffer is in the workspace
+    kw = dict(dtype=moe.MOE_BF16, T=64, E=8, k=2, I=256, x=1 << 20, W1=1 << 21, W2=1 << 22, out=1 << 23,
+              logits=1 << 24)
+    odd = moe.moe_forward_workspace_size(moe.forward_args(H=200, gather=True, **kw))
+    odd_sep = moe.moe_forward_workspace_size(moe.forward_args(H=200, **kw))
+    assert odd == odd_sep
+    gat = moe.moe_forward_workspace_size(moe.forward_args(H=256, gather=True, **kw))
+    sep = moe.moe_forward_workspace_size(moe.forward_args(H=256, **kw))
+    assert sep == gat + 64 * 2 * 256 * 2
 
 
 def test_workspace_too_small_is_reported(moe):
