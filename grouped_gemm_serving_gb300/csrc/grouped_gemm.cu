@@ -11,25 +11,41 @@
 // over rows sorted by expert id (grouped_mm backend, "Mixture of Experts in
 // transformers").
 //
-// Design (one persistent CTA per SM, 384 threads):
-//   warp 0      TMA producer: A tile [128 rows x 128 bytes] and B tile
-//               [256 rows x 128 bytes] per k-block into a 4-stage ring;
-//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32 bytes) per
-//               k-block into one of two 256-column TMEM accumulators;
-//   warps 2-3   idle (they complete warpgroup 0 for the register split),
+// Two kernels share the code below (one persistent CTA per SM, 384 threads).
+//
+// bf16 (SWAP): swapped operands on CTA pairs (clusters of two, tcgen05
+// cta_group::2).  A pair tile is 256 weight rows (128 per CTA) x the tokens of
+// one token tile of one expert (up to 256, split equally within the expert,
+// the MMA's N rounded up to 32), so the tokens of an expert pad to a multiple
+// of 32 instead of 128.  Each CTA stages its 128 weight rows and half the
+// token rows (32 KB per k-block, six deep); the even CTA issues the MMAs for
+// both and commits to both CTAs' barriers; each CTA's accumulator holds its
+// weight rows x all tokens of the tile.  SwiGLU: a CTA's weight rows are 64
+// gate rows followed by the same 64 up rows, so the epilogue warp pair that
+// holds a feature's gate and up rows swaps half of each 32-token chunk through
+// shared memory and both compute silu(g) * u.
+//
+// FP8 (and gathered A): single CTAs, 128 rows (tokens) x 256 columns
+// (weights), 48 KB per k-block, four deep.  Each 128-wide k-block is an exact
+// e4m3 x e4m3 partial in TMEM; the epilogue promotes it with
+// sa[row, kb] * sb[block, kb] into fp32 registers while the MMA fills the
+// other buffer.
+//
+// Roles:
+//   warp 0      TMA producer
+//   warp 1      MMA issuer (in a pair, the even CTA's only)
+//   warps 2-3   idle (they complete warpgroup 0 for the FP8 register split),
 //               except with gathered A (below)
 //   warps 4-11  epilogue: tcgen05.ld the accumulator, apply the epilogue and
 //               store; warp w reads TMEM lanes 32*(w%4).., columns half
 //               (w-4)/4; then zero the sentinel rows [offsets[E], M_cap).
-// The tile list is built on the device from offsets: expert e owns
-// ceil(cnt_e/128) row tiles times n_tiles column tiles, ordered expert-major,
-// then column tile, then row tile, so CTAs that run at the same time share a
-// weight tile in L2.  No tile is issued for sentinel rows.
-//
-// bf16: the accumulator sums all k-blocks of a tile in TMEM (double-buffered
-// across tiles).  FP8: each 128-wide k-block is an exact e4m3 x e4m3 partial
-// in TMEM; the epilogue promotes it with sa[row, kb] * sb[block, kb] into fp32
-// registers while the MMA fills the other buffer.
+// The producer and MMA loops run on the whole warp and let one elected lane
+// issue: TMA and tcgen05 instructions take warp-uniform operands, and issued
+// from a single-thread branch they cost several times as many cycles.
+// Accumulators are double-buffered across tiles in TMEM (2 x 256 columns).
+// The tile list is built on the device from offsets, ordered expert-major,
+// then weight tile, then token tile, so CTAs that run at the same time share
+// a weight tile in L2.  No tile is issued for sentinel rows.
 //
 // Gathered A (moe_grouped_gemm_gather): instead of one tile load from a
 // permuted buffer, the A tile is fetched four rows at a time with TMA
@@ -40,8 +56,7 @@
 // each).  This folds the scatter of "LlamaFactory Triton fused MoE kernel"
 // (section 1) into the first GEMM.  A gather4 costs far more than a quarter of
 // a 128-row tile load, and every A tile is fetched again for each column tile,
-// so this pays only when experts hold few rows (decode); with full tiles the
-// separate scatter is faster.
+// so with full tiles the separate scatter is faster.
 //
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records
 // MOE_DEVERR_TIMEOUT, stops all roles, waits (bounded) for its in-flight TMA
@@ -58,17 +73,33 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 128 + kEpiThreads;  // warpgroup 0: TMA, MMA, 2 idle warps
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kStageA = BM * 128;
 constexpr int kStageB = BN * 128;
-constexpr int kStageBytes = kStageA + kStageB;
+// Stage ring: a single-CTA tile stages 128 A + 256 B rows (48 KB) four deep;
+// a CTA of a pair stages 128 + 128 rows (32 KB) six deep, so that more loads
+// are in flight.
+constexpr int kMaxStages = 6;
+template <bool PAIR>
+struct Geo {
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kStageBytes = PAIR ? kStageA + kStageB / 2 : kStageA + kStageB;
+};
 constexpr int kMaxE = 256;
 constexpr int kScaleRing = 4;   // k-blocks of block-scale prefetch in the FP8 epilogue
 constexpr int kGatherWarps = 3; // warps 0, 2, 3 issue the row gathers of gathered A
+// Swapped operands on CTA pairs (bf16): the weights are the M = 256 rows of
+// a tcgen05 cta_group::2 MMA (128 per CTA) and an expert's tokens its N = up
+// to BT columns (N/2 rows in each CTA's shared memory), so a tile pads the
+// expert's rows to a multiple of 32 instead of 128, and each SM loads 32 KB
+// of operands per k-block instead of 48 KB.
+constexpr int BT = 256;
+constexpr int kSwapFeatSwiglu = 128;  // h features per pair tile (each CTA: 64 gate + 64 up rows)
+constexpr int kSwapFeatStore = 256;   // output features per pair tile (128 per CTA)
+constexpr bool kSwapBf16 = true;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr int kRegsLow = 56, kRegsHigh = 224;
@@ -96,7 +127,7 @@ struct Params {
 };
 
 struct Shared {
-    uint64_t full[kStages], empty[kStages];
+    uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t xbar[2];  // amax exchange of the quantising epilogue
     uint64_t mma_done;
@@ -106,16 +137,27 @@ struct Shared {
     int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
     alignas(16) int gtok[kGatherWarps][BM];  // gathered A: each issuing warp's copy of the tile's tokens
     float amax_x[2][2][BM];
-    float scale_ring[kScaleRing * 3 * kEpiThreads];   // FP8 block scales in flight
+    // swapped SwiGLU: per epilogue warp pair, channel 0 carries gate values to
+    // the up warp and channel 1 up values to the gate warp (half a chunk each)
+    uint64_t xfull[4][2], xempty[4][2];
+    union {
+        float scale_ring[kScaleRing * 3 * kEpiThreads];  // FP8 block scales in flight
+        float xch[4][2][16 * 32];
+    };
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Shared);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+    return 1024 + static_cast<size_t>(Geo<PAIR>::kStages) * Geo<PAIR>::kStageBytes + sizeof(Shared);
+}
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory per CTA");
 
 struct Tile {
     int e, row0, row_end, col0;
+    int rows;  // swapped: token rows of this tile (<= BT)
 };
 
+template <bool SWAP>
 __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params& p) {
     int lo = 0, hi = p.E;  // largest e < E with prefix[e] * n_tiles <= t
     while (hi - lo > 1) {
@@ -126,9 +168,20 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
     const int local = t - S.prefix[lo] * p.n_tiles;
     Tile ti;
     ti.e = lo;
-    ti.row0 = p.offsets[lo] + (local % mt) * BM;
     ti.row_end = p.offsets[lo + 1];
-    ti.col0 = (local / mt) * (p.half ? BN / 2 : BN);
+    if (SWAP) {
+        // an expert's tokens in mt tiles of equal size (a multiple of 32),
+        // rather than full tiles and a small remainder that would still
+        // stream the whole weight tile
+        const int cnt = ti.row_end - p.offsets[lo];
+        const int ts = ((cnt + mt - 1) / mt + 31) & ~31;
+        ti.row0 = p.offsets[lo] + (local % mt) * ts;
+        ti.rows = min(ts, ti.row_end - ti.row0);
+    } else {
+        ti.row0 = p.offsets[lo] + (local % mt) * BM;
+        ti.rows = 0;
+    }
+    ti.col0 = (local / mt) * (SWAP ? (p.half ? kSwapFeatSwiglu : kSwapFeatStore) : (p.half ? BN / 2 : BN));
     return ti;
 }
 
@@ -192,6 +245,8 @@ __device__ __forceinline__ void promote_chunk(float (&a)[128], int c, float s0, 
 }
 
 // ---------------------------------------------------------------- roles
+// The producer and MMA roles run on a whole warp: every lane tracks the ring
+// and polls the barriers, and one elected lane issues (see moe::elect_one).
 template <bool FP8, int EPI>
 __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* stages,
                          Shared& S, const Params& p, int total) {
@@ -199,36 +254,116 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     uint32_t phase = 0, issued = 0, issued_par = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile ti = decode_tile(t, S, p);
+        const Tile ti = decode_tile<false>(t, S, p);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs)) {
+            const bool got = moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             const uint32_t fb = bar(S.full[stage]);
-            moe::mbar_arrive_expect_tx(fb, kStageBytes);
-            const uint32_t sa = moe::smem_u32(stages + stage * kStageBytes);
+            const uint32_t sa = moe::smem_u32(stages + stage * Geo<false>::kStageBytes);
             const uint32_t sb = sa + kStageA;
             const int kc = kb * (FP8 ? 128 : 64);
-            moe::tma_load_2d(sa, tmA, fb, kc, ti.row0);
-            if (EPI == EPI_STORE) {
-                moe::tma_load_3d(sb, tmB, fb, kc, ti.col0, ti.e);
-            } else {
-                moe::tma_load_4d(sb, tmB, fb, kc, ti.col0, 0, ti.e);
-                moe::tma_load_4d(sb + (BN / 2) * 128, tmB, fb, kc, ti.col0, 1, ti.e);
+            if (moe::elect_one()) {
+                moe::mbar_arrive_expect_tx(fb, Geo<false>::kStageBytes);
+                moe::tma_load_2d(sa, tmA, fb, kc, ti.row0);
+                if (EPI == EPI_STORE) {
+                    moe::tma_load_3d(sb, tmB, fb, kc, ti.col0, ti.e);
+                } else {
+                    moe::tma_load_4d(sb, tmB, fb, kc, ti.col0, 0, ti.e);
+                    moe::tma_load_4d(sb + (BN / 2) * 128, tmB, fb, kc, ti.col0, 1, ti.e);
+                }
             }
+            __syncwarp();
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            if (++stage == Geo<false>::kStages) { stage = 0; phase ^= 1u; }
         }
     }
-    if (!ok) {
+    if (!ok && moe::elect_one()) {
         fail(S, p);
         int zero = 0;
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < Geo<false>::kStages; ++s)
             if ((issued >> s) & 1u)
                 moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
     }
+    __syncwarp();
+}
+
+// Token rows of a swapped tile (at most BT; the MMA's N is this rounded up to 32).
+__device__ __forceinline__ int swap_rows(const Tile& ti) { return ti.rows; }
+__device__ __forceinline__ int swap_n(const Tile& ti) { return (ti.rows + 31) & ~31; }
+
+// Tile loop bounds: a CTA pair walks the tile list as one unit.
+template <bool PAIR>
+__device__ __forceinline__ int tile_first() { return PAIR ? blockIdx.x >> 1 : blockIdx.x; }
+template <bool PAIR>
+__device__ __forceinline__ int tile_step() { return PAIR ? gridDim.x >> 1 : gridDim.x; }
+
+// Producer with swapped operands on a CTA pair (bf16).  Per k-block each CTA
+// loads its 128 weight rows into the A region and its N/2 token rows into
+// the B region, all counted on the leading CTA's full barrier (the leader
+// posts both CTAs' bytes).  SwiGLU: CTA r's weight rows are gate rows
+// col0+64r .. +63 followed by the same up rows (one box of the [E, 2, N/2, K]
+// map).  Tokens: one 128-row box (tmX128), or up to two 32-row boxes (tmX32)
+// for a half of at most 64 rows.  A TMA instruction costs the issuing thread
+// many cycles, so a k-block takes as few as possible.
+template <int EPI>
+__device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX32, const CUtensorMap* tmW,
+                              uint8_t* stages, Shared& S, const Params& p, int total, uint32_t rank) {
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int t = tile_first<true>(); ok && t < total; t += tile_step<true>()) {
+        const Tile ti = decode_tile<true>(t, S, p);
+        const int nh = swap_n(ti) / 2;                 // token rows in each CTA
+        const int nb = (nh + 31) / 32;
+        const int xbytes = nb <= 2 ? nb * 4096 : kStageB / 2;
+        const int xrow = ti.row0 + static_cast<int>(rank) * nh;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            const bool got = moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = moe::map_to_cta(bar(S.full[stage]), 0);
+            const uint32_t sa = moe::smem_u32(stages + stage * Geo<true>::kStageBytes);
+            const uint32_t sb = sa + kStageA;
+            const int kc = kb * 64;
+            if (moe::elect_one()) {
+                if (rank == 0) moe::mbar_arrive_expect_tx(bar(S.full[stage]), 2 * (kStageA + xbytes));
+                if (EPI == EPI_STORE)
+                    moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
+                else
+                    moe::tma_load_4d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 64, 0, ti.e);
+                if (nb <= 2) {
+                    for (int b = 0; b < nb; ++b)
+                        moe::tma_load_2d_pair(sb + b * 4096, tmX32, fb, kc, xrow + 32 * b);
+                } else {
+                    moe::tma_load_2d_pair(sb, tmX128, fb, kc, xrow);
+                }
+            }
+            __syncwarp();
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == Geo<true>::kStages) { stage = 0; phase ^= 1u; }
+        }
+    }
+    if (!ok && moe::elect_one()) {
+        fail(S, p);
+        int zero = 0;
+        if (rank == 0) {
+            for (int s = 0; s < Geo<true>::kStages; ++s)
+                if ((issued >> s) & 1u)
+                    moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
+        } else {
+            // the peer's loads complete on the leader's barrier: give them time to land
+            const uint64_t t0 = moe::global_timer_ns();
+            while (moe::global_timer_ns() - t0 < 1000000ull) __nanosleep(1000);
+        }
+    }
+    __syncwarp();
 }
 
 // Source token of row `row` of the permuted order, or -1 when the row is past
@@ -262,7 +397,7 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
     uint32_t phase = 0, issued = 0, issued_par = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile ti = decode_tile(t, S, p);
+        const Tile ti = decode_tile<false>(t, S, p);
         __syncwarp();  // lane 0 is done with the previous tile's tokens
 #pragma unroll
         for (int j = 0; j < BM / 32; ++j) {
@@ -280,7 +415,7 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
                     break;
                 }
                 const uint32_t fb = bar(S.full[stage]);
-                const uint32_t sa = moe::smem_u32(stages + stage * kStageBytes);
+                const uint32_t sa = moe::smem_u32(stages + stage * Geo<false>::kStageBytes);
                 const int kc = kb * (FP8 ? 128 : 64);
                 if (g == 0) {
                     moe::mbar_arrive_expect_tx(fb, kStageB + nq * 512);
@@ -314,7 +449,7 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
                 }
                 issued |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                if (++stage == Geo<false>::kStages) { stage = 0; phase ^= 1u; }
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -324,66 +459,89 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
         // this warp's gathers land whatever the other roles do; the phases
         // they count towards may never complete, so each wait is short
         int zero = 0;
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < Geo<false>::kStages; ++s)
             if ((issued >> s) & 1u)
                 moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
     }
 }
 
-template <bool FP8>
+template <bool FP8, bool SWAP>
 __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int total, uint32_t tmem) {
-    constexpr uint32_t idesc = moe::make_idesc(FP8 ? 0u : 1u, BM, BN);
+    uint32_t idesc = moe::make_idesc(FP8 ? 0u : 1u, BM, BN);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued = false;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+    for (int t = tile_first<SWAP>(); ok && t < total; t += tile_step<SWAP>()) {
+        if (SWAP) idesc = moe::make_idesc(1u, 2 * BM, swap_n(decode_tile<true>(t, S, p)));
         if (!FP8) {
-            if (!moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs)) { ok = false; break; }
+            // with a pair, the peer's epilogue arrives here from the other CTA
+            const bool got = SWAP ? moe::mbar_wait_cluster(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs)
+                                  : moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             moe::tc_fence_after();
         }
         for (int kb = 0; kb < p.k_blocks; ++kb) {
             if (FP8) {
-                if (!moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs)) { ok = false; break; }
+                const bool got = moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 moe::tc_fence_after();
             }
-            if (!moe::mbar_wait(bar(S.full[stage]), phase, &S.abort_flag, kWaitNs)) { ok = false; break; }
+            const bool got = moe::mbar_wait(bar(S.full[stage]), phase, &S.abort_flag, kWaitNs);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             moe::tc_fence_after();
-            const uint32_t sa = moe::smem_u32(stages + stage * kStageBytes);
+            const uint32_t sa = moe::smem_u32(stages + stage * Geo<SWAP>::kStageBytes);
             const uint64_t adesc = moe::smem_desc_sw128(sa);
             const uint64_t bdesc = moe::smem_desc_sw128(sa + kStageA);
             const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+            // the same (lowest) lane is elected every time, so its commits
+            // track all the MMAs it issued
+            if (moe::elect_one()) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // 32 bytes of K per instruction; +2 = +32 B start address
-                if (FP8)
-                    moe::mma_fp8(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0);
-                else
-                    moe::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
-            moe::tc_commit(bar(S.empty[stage]));
+                for (int k = 0; k < 4; ++k)  // 32 bytes of K per instruction; +2 = +32 B start address
+                    if (FP8)
+                        moe::mma_fp8(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0);
+                    else if (SWAP)
+                        moe::mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                    else
+                        moe::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                if (SWAP) moe::tc_commit_pair(bar(S.empty[stage]), 0x3);   // frees the stage in both CTAs
+                else moe::tc_commit(bar(S.empty[stage]));
+                if (FP8) moe::tc_commit(bar(S.acc_full[acc]));
+            }
+            __syncwarp();
             issued = true;
-            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            if (++stage == Geo<SWAP>::kStages) { stage = 0; phase ^= 1u; }
             if (FP8) {
-                moe::tc_commit(bar(S.acc_full[acc]));
                 acc ^= 1;
                 if (!acc) acc_phase ^= 1u;
             }
         }
         if (!ok) break;
         if (!FP8) {
-            moe::tc_commit(bar(S.acc_full[acc]));
+            if (moe::elect_one()) {
+                if (SWAP) moe::tc_commit_pair(bar(S.acc_full[acc]), 0x3);
+                else moe::tc_commit(bar(S.acc_full[acc]));
+            }
+            __syncwarp();
             acc ^= 1;
             if (!acc) acc_phase ^= 1u;
         }
     }
-    if (!ok) fail(S, p);
-    if (issued) {  // every MMA of this CTA has finished before TMEM is freed
+    if (!ok && moe::elect_one()) fail(S, p);
+    __syncwarp();
+    if (issued) {  // every MMA of this CTA (pair) has finished before TMEM is freed
         int zero = 0;
-        moe::tc_commit(bar(S.mma_done));
+        if (moe::elect_one()) {
+            if (SWAP) moe::tc_commit_pair(bar(S.mma_done), 0x1);
+            else moe::tc_commit(bar(S.mma_done));
+        }
+        __syncwarp();
         moe::mbar_wait(bar(S.mma_done), 0, &zero, kDrainNs);
     }
 }
 
-template <bool FP8, int EPI>
-__device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
+template <bool FP8, int EPI, bool SWAP>
+__device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int hsel = (warp - 4) >> 2;     // which half of the tile's columns
@@ -391,13 +549,81 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem) {
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int acc = 0, xsel = 0;
     uint32_t acc_phase = 0, xphase = 0;
+    const int xp = (q & 1) + 2 * hsel;   // swapped SwiGLU: warp pair (gate q, up q + 2) of this column half
+    uint32_t xph = 0;
     const int KB = p.k_blocks;
 
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const Tile ti = decode_tile(t, S, p);
+    // the pair's MMA waits for both CTAs' epilogues on the leader's barrier
+    uint32_t acc_empty_leader[2] = {0, 0};
+    if (SWAP) {
+        acc_empty_leader[0] = moe::map_to_cta(bar(S.acc_empty[0]), 0);
+        acc_empty_leader[1] = moe::map_to_cta(bar(S.acc_empty[1]), 0);
+    }
+    for (int t = tile_first<SWAP>(); t < total; t += tile_step<SWAP>()) {
+        const Tile ti = decode_tile<SWAP>(t, S, p);
         const int row = ti.row0 + r;
         const bool live = row < ti.row_end;
-        if (!FP8) {
+        if (SWAP) {
+            // accumulator lane = weight row, column = token of the tile
+            if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
+            moe::tc_fence_after();
+            const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
+            const int ntok = swap_rows(ti);
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int col = hsel * 128 + c * 32;
+                if (col >= ntok) break;                       // the same for the whole warp
+                uint32_t v[32];
+                moe::tmem_ld32(ta + col, v);
+                moe::tmem_ld_wait();
+                if (EPI == EPI_STORE) {
+                    // one output feature per lane; a warp store covers 64
+                    // contiguous bytes of one token row
+                    const int f = ti.col0 + static_cast<int>(rank) * 128 + q * 32 + lane;
+                    if (f < p.out_cols) {
+                        __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + col) * p.out_cols + f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                } else {
+                    // gate warp (lanes 0-63) and up warp (lanes 64-127) of a
+                    // pair hold the same 32 features; each sends the other the
+                    // half of the chunk it does not compute, so the SwiGLU work
+                    // is spread evenly over the four SM sub-partitions
+                    const int r = q >= 2;                     // 0: gate warp, 1: up warp
+                    if (!moe::mbar_wait(bar(S.xempty[xp][r]), xph ^ 1u, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
+                    float* mine = S.xch[xp][r];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = __uint_as_float(v[r ? j : 16 + j]);
+                    moe::mbar_arrive(bar(S.xfull[xp][r]));
+                    if (!moe::mbar_wait(bar(S.xfull[xp][r ^ 1]), xph, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
+                    const float* theirs = S.xch[xp][r ^ 1];
+                    float h[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float o = theirs[j * 32 + lane];
+                        h[j] = r ? silu_mul(o, __uint_as_float(v[16 + j])) : silu_mul(__uint_as_float(v[j]), o);
+                    }
+                    moe::mbar_arrive(bar(S.xempty[xp][r ^ 1]));
+                    xph ^= 1u;
+                    const int f = ti.col0 + static_cast<int>(rank) * 64 + 32 * (q & 1) + lane;
+                    const int t0 = col + 16 * r;
+                    if (f < p.out_cols) {
+                        __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + t0) * p.out_cols + f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (t0 + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(h[j]);
+                    }
+                }
+            }
+            moe::tc_fence_before();
+            if (rank != 0) moe::mbar_arrive_cluster(acc_empty_leader[acc]);
+            else moe::mbar_arrive(bar(S.acc_empty[acc]));
+            acc ^= 1;
+            if (!acc) acc_phase ^= 1u;
+        } else if (!FP8) {
             if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
             moe::tc_fence_after();
             const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
@@ -587,26 +813,34 @@ __device__ void zero_sentinel_rows(const Params& p) {
     }
 }
 
-template <bool FP8, int EPI>
+template <bool FP8, int EPI, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmA128, const __grid_constant__ CUtensorMap tmA32,
                     const Params p) {
+    static_assert(!(SWAP && FP8), "swapped operands are a bf16 path");
+    const uint32_t rank = SWAP ? moe::cluster_ctarank() : 0;   // 0 leads a pair
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared& S = *reinterpret_cast<Shared*>(stages + kStages * kStageBytes);
+    Shared& S = *reinterpret_cast<Shared*>(stages + Geo<SWAP>::kStages * Geo<SWAP>::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < Geo<SWAP>::kStages; ++s) {
             moe::mbar_init(bar(S.full[s]), 1);
             moe::mbar_init(bar(S.empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             moe::mbar_init(bar(S.acc_full[a]), 1);
-            moe::mbar_init(bar(S.acc_empty[a]), kEpiThreads);
+            moe::mbar_init(bar(S.acc_empty[a]), SWAP ? 2 * kEpiThreads : kEpiThreads);
             moe::mbar_init(bar(S.xbar[a]), kEpiThreads);
         }
         moe::mbar_init(bar(S.mma_done), 1);
+        for (int i = 0; i < 4; ++i)
+            for (int c = 0; c < 2; ++c) {
+                moe::mbar_init(bar(S.xfull[i][c]), 32);
+                moe::mbar_init(bar(S.xempty[i][c]), 32);
+            }
         S.abort_flag = 0;
         moe::fence_barrier_init();
     }
@@ -620,7 +854,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (e < p.E) {
                 const int lo = p.offsets[e], hi = p.offsets[e + 1];
                 if (hi < lo) bad = 1;
-                mt[i] = hi > lo ? (hi - lo + BM - 1) / BM : 0;
+                constexpr int RT = SWAP ? BT : BM;   // rows of an expert per tile
+                mt[i] = hi > lo ? (hi - lo + RT - 1) / RT : 0;
                 sum += mt[i];
             }
         }
@@ -648,44 +883,55 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1 && lane == 0) {
         moe::prefetch_tensormap(&tmA);
         moe::prefetch_tensormap(&tmB);
+        if (SWAP) {
+            moe::prefetch_tensormap(&tmA128);
+            moe::prefetch_tensormap(&tmA32);
+        }
     }
     __syncthreads();
-    if (!S.valid) return;
+    if (!S.valid) return;   // both CTAs of a pair read the same offsets and leave together
     if (warp == 1) {
-        moe::tmem_alloc(moe::smem_u32(&S.tmem_base), kTmemCols);
-        moe::tmem_relinquish();
+        if (SWAP) {
+            moe::tmem_alloc_pair(moe::smem_u32(&S.tmem_base), kTmemCols);
+            moe::tmem_relinquish_pair();
+        } else {
+            moe::tmem_alloc(moe::smem_u32(&S.tmem_base), kTmemCols);
+            moe::tmem_relinquish();
+        }
     }
     moe::tc_fence_before();
-    __syncthreads();
+    if (SWAP) moe::cluster_sync();   // the peer's barriers exist before anyone signals them
+    else __syncthreads();
     moe::tc_fence_after();
     const uint32_t tmem = S.tmem_base;
-    const int total = S.prefix[p.E] * p.n_tiles;
+    const int total = S.prefix[p.E] * p.n_tiles;   // tiles (pair tiles when SWAP)
 
     // FP8 promotion keeps 128 fp32 accumulators per epilogue thread: move
     // registers from warpgroup 0 (TMA, MMA) to the two epilogue warpgroups.
     // 128 * kRegsLow + 256 * kRegsHigh = 384 * 168, the launch allocation.
     if (warp >= 4) {
         if (FP8) moe::reg_alloc<kRegsHigh>();
-        epilogue<FP8, EPI>(S, p, total, tmem);
+        epilogue<FP8, EPI, SWAP>(S, p, total, tmem, rank);
         zero_sentinel_rows<EPI>(p);
     } else {
         if (FP8) moe::reg_dealloc<kRegsLow>();
-        if (p.gx && (warp == 0 || warp - 1 < kGatherWarps) && warp != 1) {
+        if (!SWAP && p.gx && (warp == 0 || warp - 1 < kGatherWarps) && warp != 1) {
             producer_gather<FP8, EPI>(&tmA, &tmB, stages, S, p, total, warp == 0 ? 0 : warp - 1);
             __syncwarp();
         } else if (warp == 0) {
-            if (lane == 0) producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
-            __syncwarp();
+            if (SWAP) producer_swap<EPI>(&tmA128, &tmA32, &tmB, stages, S, p, total, rank);
+            else producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
         } else if (warp == 1) {
-            if (lane == 0) mma_issuer<FP8>(stages, S, p, total, tmem);
-            __syncwarp();
+            if (rank == 0) mma_issuer<FP8, SWAP>(stages, S, p, total, tmem);
         }
     }
     moe::tc_fence_before();
-    __syncthreads();
+    if (SWAP) moe::cluster_sync();   // no CTA of the pair leaves while its peer may still signal it
+    else __syncthreads();
     if (warp == 1) {
         moe::tc_fence_after();
-        moe::tmem_dealloc(tmem, kTmemCols);
+        if (SWAP) moe::tmem_dealloc_pair(tmem, kTmemCols);
+        else moe::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -715,9 +961,11 @@ bool encode(CUtensorMap* map, bool fp8, const void* base, int rank, const cuuint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, int EPI>
-moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p, cudaStream_t s) {
-    auto kern = grouped_gemm_kernel<FP8, EPI>;
+template <bool FP8, int EPI, bool SWAP = false>
+moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA128,
+                    const CUtensorMap& tmA32, const Params& p, cudaStream_t s) {
+    auto kern = grouped_gemm_kernel<FP8, EPI, SWAP>;
+    constexpr size_t kSmemBytes = smem_bytes<SWAP>();
     static int configured[64] = {0};
     int dev = 0;
     MOE_CHECK_CUDA(cudaGetDevice(&dev));
@@ -727,10 +975,30 @@ moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params
                                             static_cast<int>(kSmemBytes)));
         configured[dev] = 1;
     }
-    const int grid = moe::sm_count();
+    int grid = moe::sm_count();
+    if (SWAP) grid &= ~1;   // whole CTA pairs
     if (grid <= 0) return MOE_ERR_CUDA;
-    kern<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
-    MOE_CHECK_LAUNCH();
+    if (!SWAP) {
+        kern<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmA128, tmA32, p);
+        MOE_CHECK_LAUNCH();
+        return MOE_OK;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA128, tmA32, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
     return MOE_OK;
 }
 
@@ -763,25 +1031,33 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
         if ((static_cast<int64_t>(K) * esz) % 128 != 0) return MOE_ERR_UNSUPPORTED;
     }
     const int half = swiglu ? N / 2 : 0;
-    const int n_tiles = swiglu ? (half + BN / 2 - 1) / (BN / 2) : (N + BN - 1) / BN;
-    const int64_t max_tiles = (static_cast<int64_t>(M_cap) / BM + E) * n_tiles;
+    // bf16 without a gather runs with swapped operands: weight-row tiles x
+    // token tiles of up to BT rows
+    const bool swap = kSwapBf16 && !fp8 && !gx;
+    const int feat = swap ? (swiglu ? kSwapFeatSwiglu : kSwapFeatStore) : (swiglu ? BN / 2 : BN);
+    const int n_tiles = ((swiglu ? half : N) + feat - 1) / feat;
+    const int64_t max_tiles = (static_cast<int64_t>(M_cap) / (swap ? BT : BM) + E) * n_tiles;
     MOE_CHECK_ARG(max_tiles < INT_MAX);
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
 
     const cuuint32_t bk = 128 / esz;  // elements in a 128-byte k-block row
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmA128, tmA32;
     {
-        // permuted A: 128-row tiles; gathered A: x [T, K] read a row at a time
+        // permuted A: 128-row tiles (swapped: token tiles in boxes of 256,
+        // 128 or 32 rows); gathered A: x [T, K] read a row at a time
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(gx ? T : M_cap)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * esz};
-        const cuuint32_t box[2] = {bk, gx ? 1u : static_cast<cuuint32_t>(BM)};
+        const cuuint32_t box[2] = {bk, gx ? 1u : swap ? static_cast<cuuint32_t>(BT) : static_cast<cuuint32_t>(BM)};
         if (!encode(&tmA, fp8, A, 2, dims, strides, box)) return MOE_ERR_CUDA;
+        const cuuint32_t box128[2] = {bk, 128u}, box32[2] = {bk, 32u};
+        if (!encode(&tmA128, fp8, A, 2, dims, strides, box128)) return MOE_ERR_CUDA;
+        if (!encode(&tmA32, fp8, A, 2, dims, strides, box32)) return MOE_ERR_CUDA;
     }
     if (!swiglu) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(N) * K * esz};
-        const cuuint32_t box[3] = {bk, BN, 1};
+        const cuuint32_t box[3] = {bk, swap ? 128u : BN, 1};   // swapped: 128 weight rows per CTA
         if (!encode(&tmB, fp8, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
     } else {
         // [E, 2, N/2, K]: a gate box clips at N/2 instead of running into the up rows
@@ -789,7 +1065,8 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
                                     static_cast<cuuint64_t>(E)};
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(half) * K * esz,
                                        static_cast<cuuint64_t>(N) * K * esz};
-        const cuuint32_t box[4] = {bk, BN / 2, 1, 1};
+        // swapped: 64 gate rows and the same 64 up rows per box (per CTA)
+        const cuuint32_t box[4] = {bk, swap ? 64u : BN / 2, swap ? 2u : 1u, 1};
         if (!encode(&tmB, fp8, B, 4, dims, strides, box)) return MOE_ERR_CUDA;
     }
 
@@ -815,12 +1092,16 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     p.topk = gx ? topk : 1;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fp8) {
-        if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, p, s);
-        if (epilogue == MOE_EPI_SWIGLU) return launch<true, EPI_SWIGLU>(tmA, tmB, p, s);
-        return launch<true, EPI_SWIGLU_Q>(tmA, tmB, p, s);
+        if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
+        if (epilogue == MOE_EPI_SWIGLU) return launch<true, EPI_SWIGLU>(tmA, tmB, tmA128, tmA32, p, s);
+        return launch<true, EPI_SWIGLU_Q>(tmA, tmB, tmA128, tmA32, p, s);
     }
-    if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE>(tmA, tmB, p, s);
-    return launch<false, EPI_SWIGLU>(tmA, tmB, p, s);
+    if (swap) {
+        if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE, true>(tmA, tmB, tmA128, tmA32, p, s);
+        return launch<false, EPI_SWIGLU, true>(tmA, tmB, tmA128, tmA32, p, s);
+    }
+    if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
+    return launch<false, EPI_SWIGLU>(tmA, tmB, tmA128, tmA32, p, s);
 }
 
 }  // namespace
