@@ -22,12 +22,14 @@ __device__ __forceinline__ int live_rows(const int32_t* offsets, int E, int M_ca
     return L;
 }
 
-// xp[p] = x[sorted_rows[p] / k] for p < L; one warp per row, persistent over rows.
-// row_vecs = bytes per row / 16.  FP8 rows also move their group scales into
-// the group-major layout xp_scales[g * M_cap + p].
+// xp[p] = x[sorted_rows[p] / k] for p < L; one warp per (row, segment),
+// persistent over them.  row_vecs = bytes per row / 16; a row is split into
+// segs segments of seg_vecs vectors (segs = 1 unless there are too few rows
+// to fill the GPU).  FP8 rows also move their group scales into the
+// group-major layout xp_scales[g * M_cap + p].
 __global__ void __launch_bounds__(kThreads)
 permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, int T, int k,
-               int row_vecs, int G, const int32_t* __restrict__ sorted_rows,
+               int row_vecs, int segs, int seg_vecs, int G, const int32_t* __restrict__ sorted_rows,
                const int32_t* __restrict__ offsets, int E, int M_cap, uint4* __restrict__ xp,
                float* __restrict__ xp_scales, int* err) {
     const int L = live_rows(offsets, E, M_cap, err);
@@ -35,18 +37,22 @@ permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, 
     const int lane = threadIdx.x & 31;
     const int warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kWarpsPerBlock;
-    for (int p = warp0; p < L; p += nwarps) {
+    const int64_t n = static_cast<int64_t>(L) * segs;
+    for (int64_t w = warp0; w < n; w += nwarps) {
+        const int p = static_cast<int>(w / segs);
+        const int seg = static_cast<int>(w - static_cast<int64_t>(p) * segs);
         const int slot = sorted_rows[p];
         const int t = slot / k;
         if (slot < 0 || t >= T) {
-            moe::raise_device_error(err, MOE_DEVERR_ROUTE);
+            if (seg == 0) moe::raise_device_error(err, MOE_DEVERR_ROUTE);
             continue;
         }
         const uint4* src = x + static_cast<int64_t>(t) * row_vecs;
         uint4* dst = xp + static_cast<int64_t>(p) * row_vecs;
+        const int v_end = min(row_vecs, (seg + 1) * seg_vecs);
 #pragma unroll 8
-        for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
-        if (x_scales)
+        for (int i = seg * seg_vecs + lane; i < v_end; i += 32) dst[i] = __ldg(src + i);
+        if (x_scales && seg == 0)
             for (int g = lane; g < G; g += 32)
                 xp_scales[static_cast<int64_t>(g) * M_cap + p] = __ldg(x_scales + static_cast<int64_t>(t) * G + g);
     }
@@ -148,6 +154,90 @@ combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
     }
 }
 
+// The same sum for small T, with several warps per token so that the grid
+// still fills the GPU: warp w handles token w / segs, vectors
+// [seg * seg_vecs, ...) of its row.  Same arithmetic and order per element.
+constexpr int kCombineChunks = 1;
+
+__global__ void __launch_bounds__(kThreads)
+combine_split_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
+               const float* __restrict__ w, const int32_t* __restrict__ row_pos, int T, int k,
+               int row_vecs, int segs, int seg_vecs, int E, int64_t M_cap, uint4* __restrict__ out,
+               int* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int t = static_cast<int>(gw / segs);
+    const int seg = static_cast<int>(gw - static_cast<int64_t>(t) * segs);
+    if (t >= T) return;
+    // lane j < k holds slot j's row (or -1) and weight
+    int my_row = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        const int64_t f = static_cast<int64_t>(t) * k + lane;
+        const int id = ids[f];
+        if (id != E) {
+            const int pos = row_pos[f];
+            if (pos < 0 || pos >= M_cap) {
+                if (seg == 0) moe::raise_device_error(err, MOE_DEVERR_ROUTE);
+            } else {
+                my_row = pos;
+                my_w = w[f];
+            }
+        }
+    }
+    uint4* dst = out + static_cast<int64_t>(t) * row_vecs;
+    const int v_end = min(row_vecs, (seg + 1) * seg_vecs);
+    // The trip counts are the same for every lane, so the shuffles see a full
+    // warp.  Up to KG slots' vectors of every chunk are loaded before any is
+    // used; they are then accumulated in slot order.
+    constexpr int KG = 8, CH = kCombineChunks;
+    for (int c0 = seg * seg_vecs; c0 < v_end; c0 += 32 * CH) {
+        float acc[CH][8];
+#pragma unroll
+        for (int h = 0; h < CH; ++h)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
+        for (int j0 = 0; j0 < k; j0 += KG) {
+            uint4 v[KG][CH];
+            float wj[KG];
+            bool use[KG];
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+                const int j = j0 + g;
+                const int row = __shfl_sync(0xffffffffu, my_row, j & 31);
+                wj[g] = __shfl_sync(0xffffffffu, my_w, j & 31);
+                use[g] = j < k && row >= 0;   // sentinel slots are skipped
+#pragma unroll
+                for (int h = 0; h < CH; ++h) {
+                    const int c = c0 + 32 * h + lane;
+                    v[g][h] = use[g] && c < v_end ? __ldg(Y2 + static_cast<int64_t>(row) * row_vecs + c)
+                                                  : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+                if (!use[g]) continue;
+#pragma unroll
+                for (int h = 0; h < CH; ++h) {
+                    const uint32_t vs[4] = {v[g][h].x, v[g][h].y, v[g][h].z, v[g][h].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[h][2 * i] = fmaf(wj[g], moe::bf16_lo(vs[i]), acc[h][2 * i]);
+                        acc[h][2 * i + 1] = fmaf(wj[g], moe::bf16_hi(vs[i]), acc[h][2 * i + 1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < CH; ++h) {
+            const int c = c0 + 32 * h + lane;
+            if (c < v_end)
+                dst[c] = make_uint4(moe::pack_bf16x2(acc[h][0], acc[h][1]), moe::pack_bf16x2(acc[h][2], acc[h][3]),
+                                    moe::pack_bf16x2(acc[h][4], acc[h][5]), moe::pack_bf16x2(acc[h][6], acc[h][7]));
+        }
+    }
+}
+
 int persistent_blocks(int64_t work_warps) {
     const int64_t want = (work_warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t cap = static_cast<int64_t>(moe::sm_count() > 0 ? moe::sm_count() : 148) * 8;
@@ -176,8 +266,16 @@ extern "C" moe_status_t moe_permute(moe_dtype_t dtype, const void* x, const floa
     }
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
-    permute_kernel<<<persistent_blocks(M_cap), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(x), fp8 ? x_scales : nullptr, T, k, row_vecs, G, sorted_rows,
+    // fewer rows than 8 warps per SM: split rows into segments of whole
+    // 32-vector chunks until there are ~32 warps per SM
+    const int sm = moe::sm_count() > 0 ? moe::sm_count() : 148;
+    const int max_segs = (row_vecs + 31) / 32;
+    const int64_t want = M_cap < sm * kWarpsPerBlock ? (static_cast<int64_t>(sm) * 32 + M_cap - 1) / M_cap : 1;
+    const int segs = static_cast<int>(want < max_segs ? (want > 1 ? want : 1) : max_segs);
+    const int seg_vecs = ((row_vecs + segs - 1) / segs + 31) / 32 * 32;
+    permute_kernel<<<persistent_blocks(static_cast<int64_t>(M_cap) * segs), kThreads, 0,
+                     reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(x), fp8 ? x_scales : nullptr, T, k, row_vecs, segs, seg_vecs, G, sorted_rows,
         offsets, E, M_cap, static_cast<uint4*>(xp), fp8 ? xp_scales : nullptr, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
@@ -205,9 +303,24 @@ extern "C" moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, con
     MOE_CHECK_ARG(moe::aligned16(Y2) && moe::aligned16(out));
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
-    const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    combine_kernel<<<blocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(Y2), topk_ids, topk_w, row_pos, T, k, H / 8, E,
+    const int sm = moe::sm_count() > 0 ? moe::sm_count() : 148;
+    if (T >= sm * kWarpsPerBlock) {   // at least a block of tokens per SM: one warp per token
+        const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+        combine_kernel<<<blocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint4*>(Y2), topk_ids, topk_w, row_pos, T, k, H / 8, E,
+            static_cast<int64_t>(T) * k, static_cast<uint4*>(out), err);
+        MOE_CHECK_LAUNCH();
+        return MOE_OK;
+    }
+    // few tokens: split each row over warps until the grid has ~32 warps per SM
+    const int row_vecs = H / 8, step = 32 * kCombineChunks;
+    const int max_segs = (row_vecs + step - 1) / step;
+    const int64_t want = (static_cast<int64_t>(sm) * 32 + T - 1) / T;
+    const int segs = static_cast<int>(want < max_segs ? (want > 1 ? want : 1) : max_segs);
+    const int seg_vecs = ((row_vecs + segs - 1) / segs + step - 1) / step * step;
+    const int64_t blocks = (static_cast<int64_t>(T) * segs + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    combine_split_kernel<<<static_cast<int>(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(Y2), topk_ids, topk_w, row_pos, T, k, row_vecs, segs, seg_vecs, E,
         static_cast<int64_t>(T) * k, static_cast<uint4*>(out), err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
