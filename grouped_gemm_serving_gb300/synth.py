@@ -83,6 +83,9 @@ WORKLOADS = {
     # 256-expert top-8 fine-grained FP8 layer, H=7168, I=2048
     "256e-top8-h7168-fp8": Workload("256e-top8-h7168-fp8", T=4096, E=256, k=8, H=7168,
                                     I=2048, dtype="fp8"),
+    # decode-sized batch of the FP8 layer: 64 tokens
+    "256e-top8-h7168-fp8-t64": Workload("256e-top8-h7168-fp8-t64", T=64, E=256, k=8, H=7168,
+                                        I=2048, dtype="fp8"),
 }
 
 

@@ -140,3 +140,32 @@ def test_deterministic(moe):
         moe.moe_grouped_gemm(moe.MOE_BF16, A, None, B, None, dev(off), E, M_cap, N, K, moe.MOE_EPI_STORE, C, None)
         outs.append(host_bf16_bits(C))
     assert np.array_equal(outs[0], outs[1])
+
+
+# bf16 runs with swapped operands on CTA pairs: an expert's tokens form
+# ceil(cnt/256) equal tiles rounded up to 32 rows.  Expert sizes around those
+# boundaries (1, 31-33, 255-257, 512-513 rows, several tiles) for both
+# epilogues, with an N tail and K not a multiple of the 64-element k-block.
+PAIR_COUNTS = [1, 31, 32, 33, 255, 256, 257, 512, 513, 700, 0, 1500]
+
+
+@pytest.mark.parametrize("epi", ["store", "swiglu"])
+def test_bf16_token_tile_boundaries(moe, epi):
+    E = len(PAIR_COUNTS)
+    off = np.concatenate([[0], np.cumsum(PAIR_COUNTS)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap, K = live + 40, 200
+    N = 392 if epi == "store" else 2 * 200
+    A = synth.grouped_rows(M_cap, K, live, seed=77)
+    B = _weights(E, N, K, 8)
+    ref = oracle.grouped_gemm_bf16(A, B, off)
+    if epi == "swiglu":
+        ref = oracle.swiglu(ref, live)
+    ncol = N if epi == "store" else N // 2
+    C = torch.full((M_cap, ncol), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, dev_bf16(A), None, dev_bf16(B), None, dev(off), E, M_cap, N, K,
+                         moe.MOE_EPI_STORE if epi == "store" else moe.MOE_EPI_SWIGLU, C, None)
+    assert moe.moe_get_device_error() == 0
+    got = host_f32_from_bf16(C)
+    assert_close_bf16(got[:live], ref[:live])
+    assert np.all(host_bf16_bits(C)[live:] == 0)
