@@ -286,6 +286,54 @@ void orc_grouped_gemm_bf16(const uint16_t* A, const uint16_t* B, const int32_t* 
     }
 }
 
+// Gradients of the bf16 grouped GEMM C[p, n] = sum_c A[p, c] B[e, n, c]
+// (rows p of expert e), for training ("Mixture of Experts in transformers",
+// MoE training with grouped GEMMs; section 3 of the transformers MoE/FP8
+// write-up: gradients of sentinel rows must be written, as zeros).  Given the
+// output gradient dC [M_cap, N] (bf16), plain chain rule, fp64 accumulation:
+//   dA[p, c] = sum_n dC[p, n] * B[e, n, c]   (rows p >= offsets[E]: 0)
+void orc_grouped_gemm_dgrad_bf16(const uint16_t* dC, const uint16_t* B, const int32_t* offsets, int E,
+                                 int64_t M_cap, int N, int K, float* dA) {
+    std::vector<double> acc(K);
+    for (int64_t p = 0; p < M_cap; ++p) {
+        float* dAp = dA + p * K;
+        const int e = expert_of_row(offsets, E, p);
+        if (e < 0) {
+            for (int c = 0; c < K; ++c) dAp[c] = 0.0f;
+            continue;
+        }
+        std::fill(acc.begin(), acc.end(), 0.0);
+        const uint16_t* Be = B + (int64_t)e * N * K;
+        for (int n = 0; n < N; ++n) {
+            const double g = bf16_to_f32(dC[p * N + n]);
+            for (int c = 0; c < K; ++c) acc[c] += g * (double)bf16_to_f32(Be[(int64_t)n * K + c]);
+        }
+        for (int c = 0; c < K; ++c) dAp[c] = static_cast<float>(acc[c]);
+    }
+}
+
+//   dB[e, n, c] = sum over rows p of expert e of dC[p, n] * A[p, c]
+// (an expert without rows gets a zero gradient).  With pairs (n_pairs > 0),
+// only the rows dB[pairs[2i], pairs[2i+1], :] are computed, into
+// dB[i * K .. i * K + K).
+void orc_grouped_gemm_wgrad_bf16(const uint16_t* A, const uint16_t* dC, const int32_t* offsets, int E,
+                                 int64_t M_cap, int N, int K, const int32_t* pairs, int64_t n_pairs,
+                                 float* dB) {
+    (void)M_cap;
+    std::vector<double> acc(K);
+    const int64_t nout = pairs ? n_pairs : (int64_t)E * N;
+    for (int64_t i = 0; i < nout; ++i) {
+        const int e = pairs ? pairs[2 * i] : (int)(i / N);
+        const int n = pairs ? pairs[2 * i + 1] : (int)(i % N);
+        std::fill(acc.begin(), acc.end(), 0.0);
+        for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+            const double g = bf16_to_f32(dC[p * N + n]);
+            for (int c = 0; c < K; ++c) acc[c] += g * (double)bf16_to_f32(A[p * K + c]);
+        }
+        for (int c = 0; c < K; ++c) dB[i * K + c] = static_cast<float>(acc[c]);
+    }
+}
+
 // FP8 grouped GEMM (grouped_fp8_matmul of section 1): A is e4m3 [M_cap, K]
 // with per-row, per-128-column scales sa [M_cap, K/128]; B is e4m3 [E, N, K]
 // with per-128x128-block scales sb [E, ceil(N/128), K/128].

@@ -19,7 +19,8 @@ _LIB = os.path.join(_HERE, "libmoe_oracle.so")
 __all__ = [
     "build", "e4m3_encode", "e4m3_decode", "bf16_round", "route_topk", "mark_sentinels",
     "sort_by_expert", "quant_act_fp8", "quant_weight_fp8", "permute", "grouped_gemm_bf16",
-    "grouped_gemm_fp8", "swiglu", "combine", "moe_forward",
+    "grouped_gemm_fp8", "swiglu", "combine", "moe_forward", "grouped_gemm_dgrad_bf16",
+    "grouped_gemm_wgrad_bf16",
 ]
 
 
@@ -147,6 +148,36 @@ def grouped_gemm_bf16(A, B, offsets, rows=None):
     _L().orc_grouped_gemm_bf16(_p(A), _p(B), _p(off), E, C.c_int64(M_cap), N, K, _p(rows),
                                C.c_int64(0 if rows is None else rows.size), _p(Cm))
     return Cm
+
+
+def grouped_gemm_dgrad_bf16(dC, B, offsets):
+    """dA [M_cap, K] fp32 of C = A B[e]^T given dC (bf16 bits [M_cap, N])."""
+    dC = _c(dC, np.uint16)
+    B = _c(B, np.uint16)
+    off = _c(offsets, np.int32)
+    M_cap, N = dC.shape
+    E, N2, K = B.shape
+    assert N == N2 and off.size == E + 1
+    dA = np.empty((M_cap, K), np.float32)
+    _L().orc_grouped_gemm_dgrad_bf16(_p(dC), _p(B), _p(off), E, C.c_int64(M_cap), N, K, _p(dA))
+    return dA
+
+
+def grouped_gemm_wgrad_bf16(A, dC, offsets, E: int, pairs=None):
+    """dB [E, N, K] fp32 of C = A B[e]^T given A and dC (bf16 bits); with
+    pairs (int32 [n, 2] of (expert, row of B)) only those rows, [n, K]."""
+    A = _c(A, np.uint16)
+    dC = _c(dC, np.uint16)
+    off = _c(offsets, np.int32)
+    M_cap, K = A.shape
+    M2, N = dC.shape
+    assert M_cap == M2 and off.size == E + 1
+    pr = _c(pairs, np.int32)
+    n = 0 if pr is None else pr.shape[0]
+    dB = np.empty((n, K) if pr is not None else (E, N, K), np.float32)
+    _L().orc_grouped_gemm_wgrad_bf16(_p(A), _p(dC), _p(off), E, C.c_int64(M_cap), N, K, _p(pr),
+                                     C.c_int64(n), _p(dB))
+    return dB
 
 
 def grouped_gemm_fp8(qa, sa, qb, sb, offsets, rows=None):
