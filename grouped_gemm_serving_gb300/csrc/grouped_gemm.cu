@@ -68,6 +68,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace {
 
@@ -124,6 +125,11 @@ struct Params {
     const uint8_t* gx;
     const int32_t* sorted_rows;
     int T, topk;
+    // weight-gradient mode (single CTA, bf16 store): A is [wg_rows, P] and B
+    // [N, P], both with each expert's rows laid out along P from a 64-aligned
+    // start, zero-padded; expert e's tile rows are all wg_rows rows and its K
+    // range its own k-blocks; the output is [E, wg_rows, N].
+    int wg, wg_rows;
 };
 
 struct Shared {
@@ -135,6 +141,7 @@ struct Shared {
     int abort_flag;
     int valid;
     int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
+    int kpre[kMaxE + 1];    // weight-gradient mode: exclusive prefix of k-blocks
     alignas(16) int gtok[kGatherWarps][BM];  // gathered A: each issuing warp's copy of the tile's tokens
     float amax_x[2][2][BM];
     // swapped SwiGLU: per epilogue warp pair, channel 0 carries gate values to
@@ -155,6 +162,7 @@ static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1
 struct Tile {
     int e, row0, row_end, col0;
     int rows;  // swapped: token rows of this tile (<= BT)
+    int kb0, nkb;  // the tile's k-blocks: [kb0, kb0 + nkb)
 };
 
 template <bool SWAP>
@@ -169,7 +177,17 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
     Tile ti;
     ti.e = lo;
     ti.row_end = p.offsets[lo + 1];
-    if (SWAP) {
+    ti.kb0 = 0;
+    ti.nkb = p.k_blocks;
+    if (!SWAP && p.wg) {
+        // weight gradient: every expert has the same output row tiles; its
+        // K range is its own zero-padded run of k-blocks
+        ti.row0 = (local % mt) * BM;
+        ti.row_end = p.wg_rows;
+        ti.rows = 0;
+        ti.kb0 = S.kpre[lo];
+        ti.nkb = S.kpre[lo + 1] - S.kpre[lo];
+    } else if (SWAP) {
         // an expert's tokens in mt tiles of equal size (a multiple of 32),
         // rather than full tiles and a small remainder that would still
         // stream the whole weight tile
@@ -255,7 +273,7 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
         const Tile ti = decode_tile<false>(t, S, p);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < ti.nkb; ++kb) {
             const bool got = moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
@@ -264,11 +282,13 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
             const uint32_t fb = bar(S.full[stage]);
             const uint32_t sa = moe::smem_u32(stages + stage * Geo<false>::kStageBytes);
             const uint32_t sb = sa + kStageA;
-            const int kc = kb * (FP8 ? 128 : 64);
+            const int kc = (ti.kb0 + kb) * (FP8 ? 128 : 64);
             if (moe::elect_one()) {
                 moe::mbar_arrive_expect_tx(fb, Geo<false>::kStageBytes);
                 moe::tma_load_2d(sa, tmA, fb, kc, ti.row0);
-                if (EPI == EPI_STORE) {
+                if (EPI == EPI_STORE && p.wg) {
+                    moe::tma_load_2d(sb, tmB, fb, kc, ti.col0);
+                } else if (EPI == EPI_STORE) {
                     moe::tma_load_3d(sb, tmB, fb, kc, ti.col0, ti.e);
                 } else {
                     moe::tma_load_4d(sb, tmB, fb, kc, ti.col0, 0, ti.e);
@@ -480,7 +500,10 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             moe::tc_fence_after();
         }
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        // weight-gradient tiles of an expert without rows have no k-blocks:
+        // the accumulator is committed untouched and the epilogue writes zeros
+        const int nkb = !SWAP && p.wg ? decode_tile<false>(t, S, p).nkb : p.k_blocks;
+        for (int kb = 0; kb < nkb; ++kb) {
             if (FP8) {
                 const bool got = moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -627,13 +650,20 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
             moe::tc_fence_after();
             const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.out_cols;
+            // weight gradient: expert e's output rows start at e * wg_rows
+            const int64_t orow_idx = p.wg ? static_cast<int64_t>(ti.e) * p.wg_rows + row : row;
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + orow_idx * p.out_cols;
             if (EPI == EPI_STORE) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[32];
-                    moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
-                    moe::tmem_ld_wait();
+                    if (ti.nkb > 0) {
+                        moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
+                        moe::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
                     if (live) store_bf16x32(orow, ti.col0 + hsel * 128 + c * 32, p.out_cols,
                                             reinterpret_cast<const float*>(v));
                 }
@@ -846,16 +876,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     if (warp == 0) {
         // validate offsets and build the row-tile prefix (8 experts per lane)
-        int mt[8], sum = 0, bad = 0;
+        int mt[8], kbl[8], sum = 0, ksum = 0, bad = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = lane * 8 + i;
             mt[i] = 0;
+            kbl[i] = 0;
             if (e < p.E) {
                 const int lo = p.offsets[e], hi = p.offsets[e + 1];
                 if (hi < lo) bad = 1;
                 constexpr int RT = SWAP ? BT : BM;   // rows of an expert per tile
                 mt[i] = hi > lo ? (hi - lo + RT - 1) / RT : 0;
+                if (!SWAP && p.wg) {   // every expert: all output row tiles; k-blocks of its rows
+                    mt[i] = (p.wg_rows + BM - 1) / BM;
+                    kbl[i] = hi > lo ? (hi - lo + 63) / 64 : 0;
+                    ksum += kbl[i];
+                }
                 sum += mt[i];
             }
         }
@@ -876,6 +912,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (e < p.E) { S.prefix[e] = run; run += mt[i]; }
         }
         if (lane == 31) S.prefix[p.E] = incl;
+        if (!SWAP && p.wg) {
+            int kincl = ksum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, kincl, off);
+                if (lane >= off) kincl += o;
+            }
+            int krun = kincl - ksum;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane * 8 + i;
+                if (e < p.E) { S.kpre[e] = krun; krun += kbl[i]; }
+            }
+            if (lane == 31) S.kpre[p.E] = kincl;
+        }
         if (lane == 0) {
             S.valid = !bad;
             if (bad && blockIdx.x == 0) moe::raise_device_error(p.err, MOE_DEVERR_OFFSETS);
@@ -912,7 +963,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp >= 4) {
         if (FP8) moe::reg_alloc<kRegsHigh>();
         epilogue<FP8, EPI, SWAP>(S, p, total, tmem, rank);
-        zero_sentinel_rows<EPI>(p);
+        if (!p.wg) zero_sentinel_rows<EPI>(p);
     } else {
         if (FP8) moe::reg_dealloc<kRegsLow>();
         if (!SWAP && p.gx && (warp == 0 || warp - 1 < kGatherWarps) && warp != 1) {
@@ -1090,6 +1141,8 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     p.sorted_rows = sorted_rows;
     p.T = gx ? T : 0;
     p.topk = gx ? topk : 1;
+    p.wg = 0;
+    p.wg_rows = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fp8) {
         if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
@@ -1105,6 +1158,45 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
 }
 
 }  // namespace
+
+moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, const int32_t* offsets, int E,
+                             int M_cap, int N, int K, void* dB, cudaStream_t s) {
+    MOE_CHECK_ARG(At_g && Bt_g && offsets && dB && E >= 1 && E <= kMaxE && M_cap >= 1);
+    MOE_CHECK_ARG(N >= 8 && N % 8 == 0 && K >= 8 && K % 8 == 0 && P >= 64 && P % 64 == 0);
+    MOE_CHECK_ARG(P < INT_MAX && static_cast<int64_t>(E) * N < INT_MAX);
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
+    CUtensorMap tmA, tmB;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
+        const cuuint32_t box[2] = {64, BM};
+        if (!encode(&tmA, false, At_g, 2, dims, strides, box)) return MOE_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(K)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
+        const cuuint32_t box[2] = {64, BN};
+        if (!encode(&tmB, false, Bt_g, 2, dims, strides, box)) return MOE_ERR_CUDA;
+    }
+    Params p{};
+    p.offsets = offsets;
+    p.out = dB;
+    p.err = err;
+    p.E = E;
+    p.M_cap = M_cap;
+    p.N = K;
+    p.K = 64;
+    p.half = 0;
+    p.out_cols = K;
+    p.n_tiles = (K + BN - 1) / BN;
+    p.k_blocks = 0;
+    p.nb_scale = 0;
+    p.topk = 1;
+    p.wg = 1;
+    p.wg_rows = N;
+    return launch<false, EPI_STORE>(tmA, tmB, tmA, tmA, p, s);
+}
 
 extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,
                                          const void* B, const float* B_scales, const int32_t* offsets,

@@ -55,6 +55,10 @@ _SIGS = {
     "moe_permute": (_S, [_I, _P, _P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm": (_S, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm_gather": (_S, [_I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_grouped_gemm_dgrad_workspace_size": (C.c_size_t, [_I, _I, _I]),
+    "moe_grouped_gemm_dgrad": (_S, [_P, _P, _P, _I, _I, _I, _I, _P, _P, C.c_size_t, _P]),
+    "moe_grouped_gemm_wgrad_workspace_size": (C.c_size_t, [_I, _I, _I, _I]),
+    "moe_grouped_gemm_wgrad": (_S, [_P, _P, _P, _I, _I, _I, _I, _P, _P, C.c_size_t, _P]),
     "moe_swiglu": (_S, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_combine": (_S, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_forward_workspace_size": (_Z, [C.POINTER(ForwardArgs)]),
@@ -172,6 +176,24 @@ def moe_grouped_gemm_gather(dtype, x, x_scales, T, k, sorted_rows, B, B_scales, 
                                          _p(offsets), E, M_cap, N, K, epilogue, _p(Cout), _p(C_scales),
                                          _stream(stream)),
            "moe_grouped_gemm_gather")
+
+
+def moe_grouped_gemm_dgrad_workspace_size(E, N, K) -> int:
+    return lib().moe_grouped_gemm_dgrad_workspace_size(E, N, K)
+
+
+def moe_grouped_gemm_dgrad(dC, B, offsets, E, M_cap, N, K, dA, ws, ws_bytes, stream=None):
+    _check(lib().moe_grouped_gemm_dgrad(_p(dC), _p(B), _p(offsets), E, M_cap, N, K, _p(dA), _p(ws), ws_bytes,
+                                        _stream(stream)), "moe_grouped_gemm_dgrad")
+
+
+def moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K) -> int:
+    return lib().moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K)
+
+
+def moe_grouped_gemm_wgrad(A, dC, offsets, E, M_cap, N, K, dB, ws, ws_bytes, stream=None):
+    _check(lib().moe_grouped_gemm_wgrad(_p(A), _p(dC), _p(offsets), E, M_cap, N, K, _p(dB), _p(ws), ws_bytes,
+                                        _stream(stream)), "moe_grouped_gemm_wgrad")
 
 
 def moe_swiglu(Y1, offsets, E, M_cap, I, h, stream=None):

@@ -258,6 +258,39 @@ moe_status_t moe_grouped_gemm_gather(moe_dtype_t dtype, const void* x, const flo
                                      float* C_scales, moe_stream_t stream);
 
 /*
+ * Gradients of the bf16 grouped GEMM C[p, n] = sum_c A[p, c] * B[e, n, c]
+ * (rows p of expert e; moe_grouped_gemm with MOE_EPI_STORE), for training
+ * ("Mixture of Experts in transformers": MoE training on grouped GEMMs;
+ * section 3 of the transformers MoE/FP8 write-up: the gradients of sentinel
+ * rows must be written, as zeros, not left uninitialised).  bf16 in and out,
+ * fp32 accumulation; offsets as in moe_grouped_gemm (device).  No host
+ * synchronisation.
+ *
+ * moe_grouped_gemm_dgrad:  dA[p, c] = sum_n dC[p, n] * B[e, n, c] for p <
+ *   offsets[E]; rows p >= offsets[E] of dA are zeros (dC's are never read).
+ *   dC bf16 [M_cap, N]; B bf16 [E, N, K]; dA bf16 [M_cap, K].
+ *   Workspace: moe_grouped_gemm_dgrad_workspace_size(E, N, K) bytes (B
+ *   transposed).
+ * moe_grouped_gemm_wgrad:  dB[e, n, c] = sum over p in [offsets[e],
+ *   offsets[e+1]) of dC[p, n] * A[p, c]; an expert without rows gets zeros;
+ *   rows p >= offsets[E] of A and dC are never read.
+ *   A bf16 [M_cap, K]; dC bf16 [M_cap, N]; dB bf16 [E, N, K].
+ *   Workspace: moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K) bytes
+ *   (dC and A transposed, each expert's rows zero-padded to a multiple of 64).
+ * Limits: 1 <= E <= 256, N and K positive multiples of 8; offsets not a
+ *   monotone prefix from 0 to at most M_cap: MOE_DEVERR_OFFSETS, nothing
+ *   computed.  Missing or small workspace: MOE_ERR_WORKSPACE.
+ */
+size_t moe_grouped_gemm_dgrad_workspace_size(int E, int N, int K);
+moe_status_t moe_grouped_gemm_dgrad(const void* dC, const void* B, const int32_t* offsets, int E,
+                                    int M_cap, int N, int K, void* dA, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream);
+size_t moe_grouped_gemm_wgrad_workspace_size(int E, int M_cap, int N, int K);
+moe_status_t moe_grouped_gemm_wgrad(const void* A, const void* dC, const int32_t* offsets, int E,
+                                    int M_cap, int N, int K, void* dB, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream);
+
+/*
  * moe_swiglu -- standalone silu(gate) * up (LlamaFactory write-up, section
  * 1): h[p, n] = g / (1 + exp(-g)) * Y1[p, I + n] with g = Y1[p, n], for
  * p < offsets[E]; rows p >= offsets[E] of h are written as zeros.

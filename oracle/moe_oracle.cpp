@@ -292,11 +292,15 @@ void orc_grouped_gemm_bf16(const uint16_t* A, const uint16_t* B, const int32_t* 
 // write-up: gradients of sentinel rows must be written, as zeros).  Given the
 // output gradient dC [M_cap, N] (bf16), plain chain rule, fp64 accumulation:
 //   dA[p, c] = sum_n dC[p, n] * B[e, n, c]   (rows p >= offsets[E]: 0)
+// With rows (n_rows > 0), only dA[rows[i], :] is computed, into dA[i * K ..).
 void orc_grouped_gemm_dgrad_bf16(const uint16_t* dC, const uint16_t* B, const int32_t* offsets, int E,
-                                 int64_t M_cap, int N, int K, float* dA) {
+                                 int64_t M_cap, int N, int K, const int32_t* rows, int64_t n_rows,
+                                 float* dA) {
     std::vector<double> acc(K);
-    for (int64_t p = 0; p < M_cap; ++p) {
-        float* dAp = dA + p * K;
+    const int64_t nout = rows ? n_rows : M_cap;
+    for (int64_t i = 0; i < nout; ++i) {
+        const int64_t p = rows ? rows[i] : i;
+        float* dAp = dA + i * K;
         const int e = expert_of_row(offsets, E, p);
         if (e < 0) {
             for (int c = 0; c < K; ++c) dAp[c] = 0.0f;

@@ -150,16 +150,20 @@ def grouped_gemm_bf16(A, B, offsets, rows=None):
     return Cm
 
 
-def grouped_gemm_dgrad_bf16(dC, B, offsets):
-    """dA [M_cap, K] fp32 of C = A B[e]^T given dC (bf16 bits [M_cap, N])."""
+def grouped_gemm_dgrad_bf16(dC, B, offsets, rows=None):
+    """dA [M_cap, K] fp32 of C = A B[e]^T given dC (bf16 bits [M_cap, N]);
+    with rows, only those rows ([len(rows), K])."""
     dC = _c(dC, np.uint16)
     B = _c(B, np.uint16)
     off = _c(offsets, np.int32)
     M_cap, N = dC.shape
     E, N2, K = B.shape
     assert N == N2 and off.size == E + 1
-    dA = np.empty((M_cap, K), np.float32)
-    _L().orc_grouped_gemm_dgrad_bf16(_p(dC), _p(B), _p(off), E, C.c_int64(M_cap), N, K, _p(dA))
+    rows = _c(rows, np.int32)
+    nout = M_cap if rows is None else rows.size
+    dA = np.empty((nout, K), np.float32)
+    _L().orc_grouped_gemm_dgrad_bf16(_p(dC), _p(B), _p(off), E, C.c_int64(M_cap), N, K, _p(rows),
+                                     C.c_int64(0 if rows is None else rows.size), _p(dA))
     return dA
 
 

@@ -102,3 +102,11 @@ def test_wgrad_pairs_select_rows_of_the_full_result():
     part = oracle.grouped_gemm_wgrad_bf16(A, dC, off, E, pairs=pairs)
     for i, (e, n) in enumerate(pairs):
         assert np.array_equal(part[i], full[e, n])
+
+
+def test_dgrad_rows_select_rows_of_the_full_result():
+    E, M_cap, live, N, K = 4, 60, 50, 10, 12
+    off, A, B, dC = _case(E, M_cap, live, N, K, seed=41)
+    full = oracle.grouped_gemm_dgrad_bf16(dC, B, off)
+    rows = np.array([0, 7, 49, 55], np.int32)
+    assert np.array_equal(oracle.grouped_gemm_dgrad_bf16(dC, B, off, rows=rows), full[rows])
