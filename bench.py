@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of replaying a CUDA graph")
+    ap.add_argument("--grad", action="store_true",
+                    help="time the grouped GEMMs' gradients (dgrad, wgrad) instead of the forward step")
     ap.add_argument("--gather", action="store_true",
                     help="gather the gate_up GEMM's rows from token order inside the GEMM "
                          "(moe_forward's MOE_FWD_GATHER) instead of a separate permute")
@@ -415,6 +417,79 @@ def sweep_main(args, synth, torch, moe):
     return 0
 
 
+# ------------------------------------------------------------------ gradients
+def grad_main(args, wl, synth, torch, moe):
+    """Forward, dgrad (dA = dC B[e]) and wgrad (dB[e] = dC_e^T A_e) of both
+    grouped GEMMs of a bf16 layer, on the layer's own routing (the library's
+    route + sort), random activations and output gradients; L2 flushed
+    between timed calls.  Gradients cost the forward's FLOPs each."""
+    if wl.dtype != "bf16":
+        raise SystemExit("--grad: bf16 layers only")
+    pk, pk_kind = peaks()
+    dev = torch.device("cuda")
+    T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
+    R = T * k
+
+    def bf16_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    r = moe.route_sort_t(E, k, logits=torch.from_numpy(synth.router_logits(wl)).to(dev),
+                         expert_bias=None if synth.expert_bias(wl) is None else
+                         torch.from_numpy(synth.expert_bias(wl)).to(dev), renormalize=wl.renormalize)
+    off = r["offsets"]
+    live = int(off[-1].item())
+    g = torch.Generator(device="cuda").manual_seed(1)
+    X = torch.randn((R, H), device=dev, generator=g).bfloat16()
+    h = torch.randn((R, I), device=dev, generator=g).bfloat16()
+    dY1 = torch.randn((R, 2 * I), device=dev, generator=g).bfloat16()
+    dY2 = torch.randn((R, H), device=dev, generator=g).bfloat16()
+    W1, W2 = bf16_dev(synth.expert_weights(wl, "w1")), bf16_dev(synth.expert_weights(wl, "w2"))
+    out1 = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=dev)
+    out2 = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    dX, dh = torch.empty_like(X), torch.empty_like(h)
+    dW1, dW2 = torch.empty_like(W1), torch.empty_like(W2)
+    ws_n = max(moe.moe_grouped_gemm_dgrad_workspace_size(E, 2 * I, H), moe.moe_grouped_gemm_dgrad_workspace_size(E, H, I),
+               moe.moe_grouped_gemm_wgrad_workspace_size(E, R, 2 * I, H), moe.moe_grouped_gemm_wgrad_workspace_size(E, R, H, I))
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    ops = {
+        "gate_up forward": lambda: moe.moe_grouped_gemm(moe.MOE_BF16, X, None, W1, None, off, E, R, 2 * I, H,
+                                                        moe.MOE_EPI_STORE, out1, None),
+        "gate_up dgrad": lambda: moe.moe_grouped_gemm_dgrad(dY1, W1, off, E, R, 2 * I, H, dX, ws, ws_n),
+        "gate_up wgrad": lambda: moe.moe_grouped_gemm_wgrad(X, dY1, off, E, R, 2 * I, H, dW1, ws, ws_n),
+        "down forward": lambda: moe.moe_grouped_gemm(moe.MOE_BF16, h, None, W2, None, off, E, R, H, I,
+                                                     moe.MOE_EPI_STORE, out2, None),
+        "down dgrad": lambda: moe.moe_grouped_gemm_dgrad(dY2, W2, off, E, R, H, I, dh, ws, ws_n),
+        "down wgrad": lambda: moe.moe_grouped_gemm_wgrad(h, dY2, off, E, R, H, I, dW2, ws, ws_n),
+    }
+    flop = {"gate_up": 2.0 * live * 2 * I * H, "down": 2.0 * live * H * I}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rows = []
+    for name, f in ops.items():
+        for _ in range(max(3, args.warmup)):
+            f()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.fmean(ts)
+        tf = flop[name.split()[0]] / (ms * 1e-3) / 1e12
+        rows.append({"op": name, "ms": ms, "tflops": tf, "frac": tf / pk["bf16_tflops"]})
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit("device error in the gradient bench")
+    print(json.dumps({"metric": "grouped GEMM forward and gradients", "unit": "TFLOP/s",
+                      "config": {"workload": wl.name, "live_rows": live, "l2": "flushed between timed calls",
+                                 "steps": args.steps, "note": "dgrad includes the weight transpose, wgrad the "
+                                 "padded transposes of the activations and output gradients"},
+                      "peak": {"bf16_tflops": pk["bf16_tflops"], "kind": pk_kind}, "rows": rows}))
+    return 0
+
+
 # ------------------------------------------------------------------ main
 def main():
     args = parse()
@@ -438,6 +513,9 @@ def main():
     import torch
     from grouped_gemm_serving_gb300 import build as gbuild
     gbuild.build()
+    if args.grad:
+        from grouped_gemm_serving_gb300 import moe
+        return grad_main(args, wl, synth, torch, moe)
     from grouped_gemm_serving_gb300 import moe
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -20,38 +20,70 @@
 
 namespace {
 
-constexpr int kTile = 32;
+constexpr int kTile = 64;      // elements per side of a transposed tile
+constexpr int kPitch = 66;     // shared-memory row pitch in elements (33 words: fewer bank conflicts)
+constexpr int kColTiles = 8;   // column tiles per CTA of the padded transpose
 constexpr int kMaxE = 256;
 
-// Wt[e, k, n] = W[e, n, k]; 32x32 tiles through shared memory.
-__global__ void __launch_bounds__(256)
-transpose_weights_kernel(const uint16_t* __restrict__ W, int N, int K, uint16_t* __restrict__ Wt) {
-    __shared__ uint16_t tile[kTile][kTile + 1];
-    const int e = blockIdx.z, n0 = blockIdx.y * kTile, k0 = blockIdx.x * kTile;
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int64_t base = static_cast<int64_t>(e) * N * K;
-    for (int i = ty; i < kTile; i += 8) {
-        const int n = n0 + i, k = k0 + tx;
-        tile[i][tx] = n < N && k < K ? W[base + static_cast<int64_t>(n) * K + k] : 0;
+// One 64 x 64 bf16 tile: rows src_row(r) of src (or zeros), columns
+// [c0, c0 + 64) (C a multiple of 8), into dst[c0 + i][q0 + r].  16-byte global
+// loads and stores; the tile passes through shared memory as 4-byte words.
+template <class SrcRow>
+__device__ __forceinline__ void transpose_tile(const uint16_t* __restrict__ src, int64_t src_pitch, int C,
+                                               SrcRow src_row, uint16_t* __restrict__ dst, int64_t dst_pitch,
+                                               int64_t q0, int64_t q_end, int c0, uint16_t (*tile)[kPitch]) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {            // 64 rows x 8 vectors
+        const int idx = t + 256 * i, r = idx >> 3, v = idx & 7;
+        const int c = c0 + 8 * v;
+        const int64_t row = src_row(r);
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (row >= 0 && c < C) x = *reinterpret_cast<const uint4*>(src + row * src_pitch + c);
+        uint32_t* w = reinterpret_cast<uint32_t*>(&tile[r][8 * v]);
+        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
     }
     __syncthreads();
-    for (int i = ty; i < kTile; i += 8) {
-        const int k = k0 + i, n = n0 + tx;
-        if (k < K && n < N) Wt[base + static_cast<int64_t>(k) * N + n] = tile[tx][i];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {            // 64 output rows x 8 vectors
+        const int idx = t + 256 * i, cc = idx >> 3, v = idx & 7;
+        const int c = c0 + cc;
+        const int64_t q = q0 + 8 * v;
+        if (c < C && q < q_end) {
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[j] = static_cast<uint32_t>(tile[8 * v + 2 * j][cc]) |
+                       (static_cast<uint32_t>(tile[8 * v + 2 * j + 1][cc]) << 16);
+            *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(c) * dst_pitch + q) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
     }
+    __syncthreads();
+}
+
+// Wt[e, k, n] = W[e, n, k]; one 64 x 64 tile per CTA (N, K multiples of 8).
+__global__ void __launch_bounds__(256)
+transpose_weights_kernel(const uint16_t* __restrict__ W, int N, int K, uint16_t* __restrict__ Wt) {
+    __shared__ __align__(16) uint16_t tile[kTile][kPitch];
+    const int e = blockIdx.z, n0 = blockIdx.y * kTile, k0 = blockIdx.x * kTile;
+    const int64_t base = static_cast<int64_t>(e) * N * K;
+    transpose_tile(W + base, K, K, [&](int r) -> int64_t { return n0 + r < N ? n0 + r : -1; }, Wt + base, N, n0, N,
+                   k0, tile);
 }
 
 // Xt[c, q] for q in [0, P): the row of X that expert e's padded run puts at q,
 // or zero.  Expert e's run starts at poff[e] = 64 * sum_{e' < e} ceil(cnt_e'/64)
-// and holds its cnt_e rows (offsets[e] ..) followed by zeros.
+// and holds its cnt_e rows (offsets[e] ..) followed by zeros.  A CTA resolves
+// its 64 columns q to source rows once, then transposes kColTiles tiles.
 __global__ void __launch_bounds__(256)
 pad_transpose_kernel(const uint16_t* __restrict__ X, int C, const int32_t* __restrict__ offsets, int E,
                      int M_cap, int64_t P, uint16_t* __restrict__ Xt, int* err) {
     __shared__ int poff[kMaxE + 1];
     __shared__ int bad;
-    __shared__ uint16_t tile[kTile][kTile + 1];
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    if (ty == 0) {   // one warp: check offsets; prefix of the padded counts, 8 experts per lane
+    __shared__ int64_t srow[kTile];
+    __shared__ __align__(16) uint16_t tile[kTile][kPitch];
+    const int tx = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp == 0) {   // check offsets; prefix of the padded counts, 8 experts per lane
         int v[8], sum = 0, b = tx == 0 && (offsets[0] != 0 || offsets[E] > M_cap);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -82,31 +114,29 @@ pad_transpose_kernel(const uint16_t* __restrict__ X, int C, const int32_t* __res
     }
     __syncthreads();
     if (bad || poff[E] > P) {   // offsets that are not a monotone prefix within M_cap: nothing is read
-        if (blockIdx.x == 0 && blockIdx.y == 0 && tx == 0 && ty == 0) moe::raise_device_error(err, MOE_DEVERR_OFFSETS);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) moe::raise_device_error(err, MOE_DEVERR_OFFSETS);
         return;
     }
     const int64_t q0 = static_cast<int64_t>(blockIdx.x) * kTile;
-    const int c0 = blockIdx.y * kTile;
-    for (int i = ty; i < kTile; i += 8) {
-        const int64_t q = q0 + i;
-        const int c = c0 + tx;
-        uint16_t v = 0;
-        if (q < poff[E] && c < C) {
+    if (threadIdx.x < kTile) {
+        const int64_t q = q0 + threadIdx.x;
+        int64_t row = -1;
+        if (q < poff[E]) {
             int lo = 0, hi = E;   // largest e with poff[e] <= q
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
                 if (poff[mid] <= q) lo = mid; else hi = mid;
             }
             const int64_t j = q - poff[lo];
-            if (j < offsets[lo + 1] - offsets[lo]) v = X[(offsets[lo] + j) * C + c];
+            if (j < offsets[lo + 1] - offsets[lo]) row = offsets[lo] + j;
         }
-        tile[i][tx] = v;
+        srow[threadIdx.x] = row;
     }
     __syncthreads();
-    for (int i = ty; i < kTile; i += 8) {
-        const int c = c0 + i;
-        const int64_t q = q0 + tx;
-        if (c < C && q < P) Xt[static_cast<int64_t>(c) * P + q] = tile[tx][i];
+    for (int ct = 0; ct < kColTiles; ++ct) {
+        const int c0 = (blockIdx.y * kColTiles + ct) * kTile;
+        if (c0 >= C) break;
+        transpose_tile(X, C, C, [&](int r) { return srow[r]; }, Xt, P, q0, P, c0, tile);
     }
 }
 
@@ -134,7 +164,7 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const void* dC, const void* B, co
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint16_t* Bt = static_cast<uint16_t*>(ws);
     const dim3 grid((K + kTile - 1) / kTile, (N + kTile - 1) / kTile, E);
-    transpose_weights_kernel<<<grid, dim3(kTile, 8), 0, s>>>(static_cast<const uint16_t*>(B), N, K, Bt);
+    transpose_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(B), N, K, Bt);
     MOE_CHECK_LAUNCH();
     // dA = dC Bt[e]^T with Bt [E, K, N]: the forward GEMM, N and K exchanged
     return moe_grouped_gemm(MOE_BF16, dC, nullptr, Bt, nullptr, offsets, E, M_cap, K, N, MOE_EPI_STORE, dA,
@@ -162,11 +192,12 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const void* A, const void* dC, co
     MOE_CHECK_ARG(P < INT_MAX);
     uint16_t* dCt = static_cast<uint16_t*>(ws);             // [N, P]
     uint16_t* At = dCt + static_cast<int64_t>(N) * P;       // [K, P]
-    const int64_t qb = (P + kTile - 1) / kTile;
-    pad_transpose_kernel<<<dim3(static_cast<unsigned>(qb), (N + kTile - 1) / kTile), dim3(kTile, 8), 0, s>>>(
+    const int64_t qb = P / kTile;   // P is a multiple of 64
+    const int span = kTile * kColTiles;
+    pad_transpose_kernel<<<dim3(static_cast<unsigned>(qb), (N + span - 1) / span), 256, 0, s>>>(
         static_cast<const uint16_t*>(dC), N, offsets, E, M_cap, P, dCt, err);
     MOE_CHECK_LAUNCH();
-    pad_transpose_kernel<<<dim3(static_cast<unsigned>(qb), (K + kTile - 1) / kTile), dim3(kTile, 8), 0, s>>>(
+    pad_transpose_kernel<<<dim3(static_cast<unsigned>(qb), (K + span - 1) / span), 256, 0, s>>>(
         static_cast<const uint16_t*>(A), K, offsets, E, M_cap, P, At, err);
     MOE_CHECK_LAUNCH();
     return moe::wgrad_gemm(dCt, At, P, offsets, E, M_cap, N, K, dB, s);
