@@ -169,3 +169,49 @@ def test_bf16_token_tile_boundaries(moe, epi):
     got = host_f32_from_bf16(C)
     assert_close_bf16(got[:live], ref[:live])
     assert np.all(host_bf16_bits(C)[live:] == 0)
+
+
+# FP8 tiles an expert's rows 128 at a time.  Expert sizes around those
+# boundaries (and 15-17, 31-33 rows: warps whose 32 rows are partly or wholly
+# past the expert's end), for all three epilogues, with several column tiles.
+FP8_COUNTS = [1, 15, 16, 17, 31, 33, 127, 128, 129, 255, 256, 257, 300, 0, 520]
+
+
+@pytest.mark.parametrize("epi", ["store", "swiglu", "swiglu_q"])
+def test_fp8_token_tile_boundaries(moe, epi):
+    E = len(FP8_COUNTS)
+    off = np.concatenate([[0], np.cumsum(FP8_COUNTS)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap, K = live + 40, 256
+    N = 384 if epi == "store" else 2 * 256
+    A = synth.grouped_rows(M_cap, K, live, seed=78)
+    A[live:] = 0
+    qa, sa = oracle.quant_act_fp8(A)
+    qb, sb = oracle.quant_weight_fp8(_weights(E, N, K, 9))
+    ref = oracle.grouped_gemm_fp8(qa, sa, qb, sb, off)
+    args = (dev(qa), dev(np.ascontiguousarray(sa.T)), dev(qb), dev(sb), dev(off), E, M_cap, N, K)
+    if epi == "store":
+        C = torch.full((M_cap, N), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_STORE, C, None)
+        assert moe.moe_get_device_error() == 0
+        assert_close_bf16(host_f32_from_bf16(C)[:live], ref[:live], rtol=2.0 ** -7, row_atol=2e-3)
+        assert np.all(host_bf16_bits(C)[live:] == 0)
+        return
+    I = N // 2
+    ref_h = oracle.swiglu(ref, live)
+    h = torch.full((M_cap, I), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_SWIGLU, h, None)
+    assert moe.moe_get_device_error() == 0
+    assert_close_bf16(host_f32_from_bf16(h)[:live], ref_h[:live], rtol=2.0 ** -7, row_atol=2e-3)
+    assert np.all(host_bf16_bits(h)[live:] == 0)
+    if epi == "swiglu_q":
+        hq = torch.full((M_cap, I), 7, dtype=torch.uint8, device="cuda")
+        hs = torch.full((I // 128, M_cap), -1.0, dtype=torch.float32, device="cuda")
+        moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_SWIGLU_QUANT_FP8, hq, hs)
+        assert moe.moe_get_device_error() == 0
+        q2 = torch.empty((M_cap, I), dtype=torch.uint8, device="cuda")
+        s2 = torch.empty((M_cap, I // 128), dtype=torch.float32, device="cuda")
+        moe.moe_act_quant_fp8(h, M_cap, I, q2, s2)
+        assert np.array_equal(host(hq)[:live], host(q2)[:live])
+        assert np.array_equal(host(hs).T[:live], host(s2)[:live])
+        assert np.all(host(hq)[live:] == 0) and np.all(host(hs).T[live:] == 1.0)
