@@ -709,9 +709,9 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             }
             // Block scales travel through a per-thread ring of kScaleRing slots
             // in shared memory, filled by 4-byte cp.async copies (one commit
-            // group per k-block) kScaleRing k-blocks before they are used, so
-            // their global-load latency stays off the promotion's critical path
-            // and they take no registers.  Layout [slot][value][thread] keeps
+            // group per k-block) about kScaleRing k-blocks before they are
+            // used, so their global-load latency stays off the promotion's
+            // critical path and they take no registers.  Layout [slot][value][thread] keeps
             // the accesses free of bank conflicts.
             constexpr int R = kScaleRing;
             const int et = threadIdx.x - 128;                 // epilogue thread 0..255
@@ -740,7 +740,6 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                 const float sb1 = EPI != EPI_STORE ? ring[(slot * 3 + 2) * kEpiThreads + et] : 0.0f;
                 const float s0 = sa * sb0;
                 const float s1 = EPI == EPI_STORE ? s0 : sa * sb1;
-                prefetch(kb + R, slot);
                 if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
                 moe::tc_fence_after();
                 const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
@@ -770,6 +769,9 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                 moe::mbar_arrive(bar(S.acc_empty[acc]));
                 acc ^= 1;
                 if (!acc) acc_phase ^= 1u;
+                // the next copies into this slot are issued once the buffer is
+                // released: their issue cost stays off the MMA's critical path
+                prefetch(kb + R, slot);
                 promote_chunk<EPI>(a, 1, s0, s1, x0, x1);
             }
             moe::cp_async_wait<0>();
