@@ -116,6 +116,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ ranks
+def flush_l2(buf, i):
+    """Evict L2 between timed steps: write a buffer larger than L2, then read
+    it back, so that L2 is left holding clean lines and the next step does not
+    pay for writing the flush's dirty lines back to HBM."""
+    buf.fill_(i & 0xFF)
+    buf.max()
+
+
 def cross_rank_max(value: float, dist, device) -> float:
     """The largest per-rank value (the slowest rank's time); identity on one rank."""
     import torch
@@ -387,7 +395,7 @@ def sweep_main(args, synth, torch, moe):
             torch.cuda.synchronize()
             t1, t2 = [], []
             for i in range(args.steps):
-                flush.fill_(i & 0xFF)
+                flush_l2(flush, i)
                 ev[0].record()
                 run()
                 ev[2].record()
@@ -471,7 +479,7 @@ def grad_main(args, wl, synth, torch, moe):
         torch.cuda.synchronize()
         ts = []
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             e0.record()
             f()
             e1.record()
@@ -584,7 +592,7 @@ def main():
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             s0.record()
             run_step()
             s1.record()
@@ -594,7 +602,7 @@ def main():
         # per-kernel durations: K more steps launched eagerly with CUDA events
         # between the kernels on the launching stream
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             step.run(record=True)
             torch.cuda.synchronize()
             step.collect()
@@ -622,7 +630,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = []
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, i)
         e0.record()
         moe.moe_forward(fa, ws, nws)
         e1.record()
@@ -731,7 +739,7 @@ def main():
                    "bias": wl.bias, "live_rows": live, "experts_with_rows": experts_live,
                    "parallelism": f"replicas x{world} (no collective)",
                    "scatter": "separate kernel" if separate else "gathered inside the gate_up GEMM",
-                   "l2": "flushed between timed steps (256 MiB write, untimed)",
+                   "l2": "flushed between timed steps (256 MiB write, then read back; untimed)",
                    "launch": "eager C-ABI calls" if args.no_graph else "CUDA graph of the step's C-ABI calls"},
         "roofline": {"bound": "tensor",
                      "kernel": ("grouped GEMM gate_up + fused SwiGLU" if separate else
