@@ -38,8 +38,7 @@ ROUTE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("wl", ROUTE_CASES, ids=lambda w: w.name)
-def test_route_sort_bit_exact(moe, wl):
+def _check_route(moe, wl):
     logits, bias, mask = synth.router_logits(wl), synth.expert_bias(wl), synth.sentinel_mask(wl)
     ids, w = oracle.route_topk(logits, bias, wl.k, wl.renormalize)
     if mask is not None:
@@ -54,6 +53,19 @@ def test_route_sort_bit_exact(moe, wl):
     assert np.array_equal(host(r["sorted_rows"]), sr)
     assert np.array_equal(host(r["row_pos"]), rp)
     np.testing.assert_allclose(host(r["w"]), w, rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("wl", ROUTE_CASES, ids=lambda w: w.name)
+def test_route_sort_bit_exact(moe, wl):
+    _check_route(moe, wl)
+
+
+# Up to 2048 slots (T*k) form one sort block; one token more makes two.  Both
+# sides of the boundary, and a single token.
+@pytest.mark.parametrize("T", [1, 3, 511, 512, 513])
+def test_route_sort_single_block_boundary(moe, T):
+    _check_route(moe, synth.Workload(f"b{T}", T=T, E=16, k=4, H=8, I=8, n_sentinel=min(5, 4 * T - 1),
+                                     bias="normal0.5"))
 
 
 def test_route_ties_go_to_lower_expert(moe):
@@ -78,6 +90,20 @@ def test_sort_of_given_ids_with_sentinels(moe):
     assert np.array_equal(host(r["row_pos"]), rp)
     assert np.array_equal(host(r["offsets"]), off)
     assert host(r["offsets"])[-1] == (ids != E).sum()
+
+
+@pytest.mark.parametrize("T,E,k", [(300, 20, 4), (64, 256, 8), (2, 3, 3)])
+def test_sort_of_given_ids_with_sentinels_small(moe, T, E, k):
+    g = np.random.default_rng(T + E)
+    ids = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[g.random((T, k)) < 0.3] = E
+    ids[0] = E                                               # a token with no live slot
+    sr, rp, off = oracle.sort_by_expert(ids, E)
+    r = moe.route_sort_t(E, k, topk_ids=dev(ids))
+    _no_device_error(moe)
+    assert np.array_equal(host(r["sorted_rows"]), sr)
+    assert np.array_equal(host(r["row_pos"]), rp)
+    assert np.array_equal(host(r["offsets"]), off)
 
 
 def test_bad_expert_id_is_reported_not_placed(moe):
