@@ -18,7 +18,7 @@
 // one token tile of one expert (up to 256, split equally within the expert,
 // the MMA's N rounded up to 32), so the tokens of an expert pad to a multiple
 // of 32 instead of 128.  Each CTA stages its 128 weight rows and half the
-// token rows (32 KB per k-block, six deep); the even CTA issues the MMAs for
+// token rows (32 KB per k-block, six deep; seven for the store epilogue); the even CTA issues the MMAs for
 // both and commits to both CTAs' barriers; each CTA's accumulator holds its
 // weight rows x all tokens of the tile.  SwiGLU: a CTA's weight rows are 64
 // gate rows followed by the same 64 up rows, so the epilogue warp pair that
@@ -80,14 +80,19 @@ constexpr int kThreads = 128 + kEpiThreads;  // warpgroup 0: TMA, MMA, 2 idle wa
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kStageA = BM * 128;
 constexpr int kStageB = BN * 128;
+enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
+
 // Stage ring: a single-CTA tile stages 128 A + 256 B rows (48 KB) four deep;
-// a CTA of a pair stages 128 + 128 rows (32 KB) six deep, so that more loads
-// are in flight.
-constexpr int kMaxStages = 6;
-template <bool PAIR>
+// a CTA of a pair stages 128 + 128 rows (32 KB) six deep, or seven for the
+// store epilogue, which needs no shared memory beyond the ring and the
+// barriers (kAux: whether the mode-specific Aux block is allocated).  The
+// bf16 pair kernels are bound by the bytes in flight per SM.
+constexpr int kMaxStages = 7;
+template <bool PAIR, int EPI>
 struct Geo {
-    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kStages = PAIR ? (EPI == EPI_STORE ? 7 : 6) : 4;
     static constexpr int kStageBytes = PAIR ? kStageA + kStageB / 2 : kStageA + kStageB;
+    static constexpr bool kAux = !(PAIR && EPI == EPI_STORE);
 };
 constexpr int kMaxE = 256;
 constexpr int kScaleRing = 4;   // k-blocks of block-scale prefetch in the FP8 epilogue
@@ -107,8 +112,6 @@ constexpr int kRegsLow = 56, kRegsHigh = 224;
 static_assert(128 * kRegsLow + kEpiThreads * kRegsHigh <= kThreads * 168,
               "register split exceeds the launch allocation");
 static_assert(kGatherWarps >= 1 && kGatherWarps <= 3, "gathering warps are 0, 2 and 3 of warpgroup 0");
-
-enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
 
 struct Params {
     const int32_t* offsets;
@@ -132,32 +135,47 @@ struct Params {
     int wg, wg_rows;
 };
 
-struct Shared {
+// Shared memory after the stage ring: barriers and the tile list (every
+// mode), then the Aux block of the modes that need it.
+struct alignas(16) Shared {
     uint64_t full[kMaxStages], empty[kMaxStages];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t xbar[2];  // amax exchange of the quantising epilogue
     uint64_t mma_done;
+    // swapped SwiGLU: per epilogue warp pair, channel 0 carries gate values to
+    // the up warp and channel 1 up values to the gate warp (half a chunk each)
+    uint64_t xfull[4][2], xempty[4][2];
     uint32_t tmem_base;
     int abort_flag;
     int valid;
     int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
+};
+struct alignas(16) Aux {
     int kpre[kMaxE + 1];    // weight-gradient mode: exclusive prefix of k-blocks
     alignas(16) int gtok[kGatherWarps][BM];  // gathered A: each issuing warp's copy of the tile's tokens
-    float amax_x[2][2][BM];
-    // swapped SwiGLU: per epilogue warp pair, channel 0 carries gate values to
-    // the up warp and channel 1 up values to the gate warp (half a chunk each)
-    uint64_t xfull[4][2], xempty[4][2];
+    float amax_x[2][2][BM];  // quantising epilogue
     union {
         float scale_ring[kScaleRing * 3 * kEpiThreads];  // FP8 block scales in flight
-        float xch[4][2][16 * 32];
+        float xch[4][2][16 * 32];                       // swapped SwiGLU exchange
     };
 };
-
-template <bool PAIR>
-constexpr size_t smem_bytes() {
-    return 1024 + static_cast<size_t>(Geo<PAIR>::kStages) * Geo<PAIR>::kStageBytes + sizeof(Shared);
+// The Aux block sits right after Shared; only kernels whose Geo::kAux is set
+// allocate it, and only their code paths reach it.
+__device__ __forceinline__ Aux& aux(Shared& S) {
+    return *reinterpret_cast<Aux*>(reinterpret_cast<uint8_t*>(&S) + sizeof(Shared));
 }
-static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory per CTA");
+__device__ __forceinline__ const Aux& aux(const Shared& S) {
+    return *reinterpret_cast<const Aux*>(reinterpret_cast<const uint8_t*>(&S) + sizeof(Shared));
+}
+
+template <bool PAIR, int EPI>
+constexpr size_t smem_bytes() {
+    using G = Geo<PAIR, EPI>;
+    return 1024 + static_cast<size_t>(G::kStages) * G::kStageBytes + sizeof(Shared) + (G::kAux ? sizeof(Aux) : 0);
+}
+static_assert(smem_bytes<false, EPI_STORE>() <= 227 * 1024 && smem_bytes<false, EPI_SWIGLU_Q>() <= 227 * 1024 &&
+                  smem_bytes<true, EPI_STORE>() <= 227 * 1024 && smem_bytes<true, EPI_SWIGLU>() <= 227 * 1024,
+              "shared memory per CTA");
 
 struct Tile {
     int e, row0, row_end, col0;
@@ -185,8 +203,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
         ti.row0 = (local % mt) * BM;
         ti.row_end = p.wg_rows;
         ti.rows = 0;
-        ti.kb0 = S.kpre[lo];
-        ti.nkb = S.kpre[lo + 1] - S.kpre[lo];
+        ti.kb0 = aux(S).kpre[lo];
+        ti.nkb = aux(S).kpre[lo + 1] - aux(S).kpre[lo];
     } else if (SWAP) {
         // an expert's tokens in mt tiles of equal size (a multiple of 32),
         // rather than full tiles and a small remainder that would still
@@ -280,11 +298,11 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
                 break;
             }
             const uint32_t fb = bar(S.full[stage]);
-            const uint32_t sa = moe::smem_u32(stages + stage * Geo<false>::kStageBytes);
+            const uint32_t sa = moe::smem_u32(stages + stage * Geo<false, EPI>::kStageBytes);
             const uint32_t sb = sa + kStageA;
             const int kc = (ti.kb0 + kb) * (FP8 ? 128 : 64);
             if (moe::elect_one()) {
-                moe::mbar_arrive_expect_tx(fb, Geo<false>::kStageBytes);
+                moe::mbar_arrive_expect_tx(fb, Geo<false, EPI>::kStageBytes);
                 moe::tma_load_2d(sa, tmA, fb, kc, ti.row0);
                 if (EPI == EPI_STORE && p.wg) {
                     moe::tma_load_2d(sb, tmB, fb, kc, ti.col0);
@@ -298,13 +316,13 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
             __syncwarp();
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == Geo<false>::kStages) { stage = 0; phase ^= 1u; }
+            if (++stage == Geo<false, EPI>::kStages) { stage = 0; phase ^= 1u; }
         }
     }
     if (!ok && moe::elect_one()) {
         fail(S, p);
         int zero = 0;
-        for (int s = 0; s < Geo<false>::kStages; ++s)
+        for (int s = 0; s < Geo<false, EPI>::kStages; ++s)
             if ((issued >> s) & 1u)
                 moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
     }
@@ -348,7 +366,7 @@ __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX3
                 break;
             }
             const uint32_t fb = moe::map_to_cta(bar(S.full[stage]), 0);
-            const uint32_t sa = moe::smem_u32(stages + stage * Geo<true>::kStageBytes);
+            const uint32_t sa = moe::smem_u32(stages + stage * Geo<true, EPI>::kStageBytes);
             const uint32_t sb = sa + kStageA;
             const int kc = kb * 64;
             if (moe::elect_one()) {
@@ -367,14 +385,14 @@ __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX3
             __syncwarp();
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == Geo<true>::kStages) { stage = 0; phase ^= 1u; }
+            if (++stage == Geo<true, EPI>::kStages) { stage = 0; phase ^= 1u; }
         }
     }
     if (!ok && moe::elect_one()) {
         fail(S, p);
         int zero = 0;
         if (rank == 0) {
-            for (int s = 0; s < Geo<true>::kStages; ++s)
+            for (int s = 0; s < Geo<true, EPI>::kStages; ++s)
                 if ((issued >> s) & 1u)
                     moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
         } else {
@@ -412,7 +430,7 @@ template <bool FP8, int EPI>
 __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* stages,
                                 Shared& S, const Params& p, int total, int g) {
     const int lane = threadIdx.x & 31;
-    int* gtok = S.gtok[g];
+    int* gtok = aux(S).gtok[g];
     int stage = 0;
     uint32_t phase = 0, issued = 0, issued_par = 0;
     bool ok = true;
@@ -435,7 +453,7 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
                     break;
                 }
                 const uint32_t fb = bar(S.full[stage]);
-                const uint32_t sa = moe::smem_u32(stages + stage * Geo<false>::kStageBytes);
+                const uint32_t sa = moe::smem_u32(stages + stage * Geo<false, EPI>::kStageBytes);
                 const int kc = kb * (FP8 ? 128 : 64);
                 if (g == 0) {
                     moe::mbar_arrive_expect_tx(fb, kStageB + nq * 512);
@@ -469,7 +487,7 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
                 }
                 issued |= 1u << stage;
                 issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-                if (++stage == Geo<false>::kStages) { stage = 0; phase ^= 1u; }
+                if (++stage == Geo<false, EPI>::kStages) { stage = 0; phase ^= 1u; }
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -479,13 +497,13 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
         // this warp's gathers land whatever the other roles do; the phases
         // they count towards may never complete, so each wait is short
         int zero = 0;
-        for (int s = 0; s < Geo<false>::kStages; ++s)
+        for (int s = 0; s < Geo<false, EPI>::kStages; ++s)
             if ((issued >> s) & 1u)
                 moe::mbar_wait(bar(S.full[s]), (issued_par >> s) & 1u, &zero, kDrainNs);
     }
 }
 
-template <bool FP8, bool SWAP>
+template <bool FP8, int EPI, bool SWAP>
 __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int total, uint32_t tmem) {
     uint32_t idesc = moe::make_idesc(FP8 ? 0u : 1u, BM, BN);
     int stage = 0, acc = 0;
@@ -512,7 +530,7 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
             const bool got = moe::mbar_wait(bar(S.full[stage]), phase, &S.abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             moe::tc_fence_after();
-            const uint32_t sa = moe::smem_u32(stages + stage * Geo<SWAP>::kStageBytes);
+            const uint32_t sa = moe::smem_u32(stages + stage * Geo<SWAP, EPI>::kStageBytes);
             const uint64_t adesc = moe::smem_desc_sw128(sa);
             const uint64_t bdesc = moe::smem_desc_sw128(sa + kStageA);
             const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
@@ -533,7 +551,7 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
             }
             __syncwarp();
             issued = true;
-            if (++stage == Geo<SWAP>::kStages) { stage = 0; phase ^= 1u; }
+            if (++stage == Geo<SWAP, EPI>::kStages) { stage = 0; phase ^= 1u; }
             if (FP8) {
                 acc ^= 1;
                 if (!acc) acc_phase ^= 1u;
@@ -617,12 +635,12 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                     // is spread evenly over the four SM sub-partitions
                     const int r = q >= 2;                     // 0: gate warp, 1: up warp
                     if (!moe::mbar_wait(bar(S.xempty[xp][r]), xph ^ 1u, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
-                    float* mine = S.xch[xp][r];
+                    float* mine = aux(S).xch[xp][r];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = __uint_as_float(v[r ? j : 16 + j]);
                     moe::mbar_arrive(bar(S.xfull[xp][r]));
                     if (!moe::mbar_wait(bar(S.xfull[xp][r ^ 1]), xph, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
-                    const float* theirs = S.xch[xp][r ^ 1];
+                    const float* theirs = aux(S).xch[xp][r ^ 1];
                     float h[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -715,7 +733,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             // the accesses free of bank conflicts.
             constexpr int R = kScaleRing;
             const int et = threadIdx.x - 128;                 // epilogue thread 0..255
-            float* ring = S.scale_ring;
+            float* ring = aux(S).scale_ring;
             auto prefetch = [&](int kq, int slot) {
                 if (kq < KB) {
                     if (row_ok)
@@ -798,10 +816,10 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                     a[i] = __bfloat162float(__float2bfloat16_rn(silu_mul(a[i], a[64 + i])));
                     amax = fmaxf(amax, fabsf(a[i]));
                 }
-                S.amax_x[xsel][hsel][r] = amax;
+                aux(S).amax_x[xsel][hsel][r] = amax;
                 moe::mbar_arrive(bar(S.xbar[xsel]));
                 if (!moe::mbar_wait(bar(S.xbar[xsel]), xphase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
-                amax = fmaxf(amax, S.amax_x[xsel][hsel ^ 1][r]);
+                amax = fmaxf(amax, aux(S).amax_x[xsel][hsel ^ 1][r]);
                 xsel ^= 1;
                 if (!xsel) xphase ^= 1u;
                 const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
@@ -854,11 +872,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t rank = SWAP ? moe::cluster_ctarank() : 0;   // 0 leads a pair
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared& S = *reinterpret_cast<Shared*>(stages + Geo<SWAP>::kStages * Geo<SWAP>::kStageBytes);
+    Shared& S = *reinterpret_cast<Shared*>(stages + Geo<SWAP, EPI>::kStages * Geo<SWAP, EPI>::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < Geo<SWAP>::kStages; ++s) {
+        for (int s = 0; s < Geo<SWAP, EPI>::kStages; ++s) {
             moe::mbar_init(bar(S.full[s]), 1);
             moe::mbar_init(bar(S.empty[s]), 1);
         }
@@ -925,9 +943,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int e = lane * 8 + i;
-                if (e < p.E) { S.kpre[e] = krun; krun += kbl[i]; }
+                if (e < p.E) { aux(S).kpre[e] = krun; krun += kbl[i]; }
             }
-            if (lane == 31) S.kpre[p.E] = kincl;
+            if (lane == 31) aux(S).kpre[p.E] = kincl;
         }
         if (lane == 0) {
             S.valid = !bad;
@@ -975,7 +993,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (SWAP) producer_swap<EPI>(&tmA128, &tmA32, &tmB, stages, S, p, total, rank);
             else producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
         } else if (warp == 1) {
-            if (rank == 0) mma_issuer<FP8, SWAP>(stages, S, p, total, tmem);
+            if (rank == 0) mma_issuer<FP8, EPI, SWAP>(stages, S, p, total, tmem);
         }
     }
     moe::tc_fence_before();
@@ -1018,7 +1036,7 @@ template <bool FP8, int EPI, bool SWAP = false>
 moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA128,
                     const CUtensorMap& tmA32, const Params& p, cudaStream_t s) {
     auto kern = grouped_gemm_kernel<FP8, EPI, SWAP>;
-    constexpr size_t kSmemBytes = smem_bytes<SWAP>();
+    constexpr size_t kSmemBytes = smem_bytes<SWAP, EPI>();
     static int configured[64] = {0};
     int dev = 0;
     MOE_CHECK_CUDA(cudaGetDevice(&dev));
