@@ -20,8 +20,8 @@
 // of 32 instead of 128.  Each CTA stages its 128 weight rows and half the
 // token rows (32 KB per k-block, six deep; seven for the store epilogue);
 // the even CTA issues the MMAs for both and commits to both CTAs' barriers;
-// each CTA's accumulator holds its
-// weight rows x all tokens of the tile.  SwiGLU: a CTA's weight rows are 64
+// each CTA's accumulator holds its weight rows x all tokens of the tile.
+// SwiGLU: a CTA's weight rows are 64
 // gate rows followed by the same 64 up rows, so the epilogue warp pair that
 // holds a feature's gate and up rows swaps half of each 32-token chunk through
 // shared memory and both compute silu(g) * u.
