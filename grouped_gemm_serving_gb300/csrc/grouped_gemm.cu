@@ -21,10 +21,10 @@
 // token rows (32 KB per k-block, six deep; seven for the store epilogue);
 // the even CTA issues the MMAs for both and commits to both CTAs' barriers;
 // each CTA's accumulator holds its weight rows x all tokens of the tile.
-// SwiGLU: a CTA's weight rows are 64
-// gate rows followed by the same 64 up rows, so the epilogue warp pair that
-// holds a feature's gate and up rows swaps half of each 32-token chunk through
-// shared memory and both compute silu(g) * u.
+// SwiGLU: a CTA's weight rows are 64 gate rows followed by the same 64 up
+// rows, so the epilogue warp pair that holds a feature's gate and up rows
+// swaps half of each 32-token chunk through shared memory and both compute
+// silu(g) * u.
 //
 // FP8 (and gathered A): single CTAs, 128 rows (tokens) x 256 columns
 // (weights), 48 KB per k-block, four deep.  Each 128-wide k-block is an exact
