@@ -16,7 +16,9 @@ from tests.gpu_helpers import (dev, dev_bf16, host, host_bf16_bits, host_f32_fro
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-SAMPLE = {"32e-top4-h2880": 16, "128e-top8-h2048-zipf": 16, "256e-top8-h7168-fp8": 4}
+SAMPLE = {"32e-top4-h2880": 16, "128e-top8-h2048-zipf": 16, "256e-top8-h7168-fp8": 4,
+          # decode-sized batches of the same layers (64 tokens)
+          "32e-top4-h2880-t64": 16, "256e-top8-h7168-fp8-t64": 4}
 
 
 @pytest.fixture(scope="module")
