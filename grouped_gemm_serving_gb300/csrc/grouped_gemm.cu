@@ -86,14 +86,12 @@ enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
 // Stage ring: a single-CTA tile stages 128 A + 256 B rows (48 KB) four deep;
 // a CTA of a pair stages 128 + 128 rows (32 KB) six deep, or seven for the
 // store epilogue, which needs no shared memory beyond the ring and the
-// barriers (kAux: whether the mode-specific Aux block is allocated).  The
-// bf16 pair kernels are bound by the bytes in flight per SM.
+// barriers (it allocates no Aux block, see smem_bytes).
 constexpr int kMaxStages = 7;
 template <bool PAIR, int EPI>
 struct Geo {
     static constexpr int kStages = PAIR ? (EPI == EPI_STORE ? 7 : 6) : 4;
     static constexpr int kStageBytes = PAIR ? kStageA + kStageB / 2 : kStageA + kStageB;
-    static constexpr bool kAux = !(PAIR && EPI == EPI_STORE);
 };
 constexpr int kMaxE = 256;
 constexpr int kScaleRing = 4;   // k-blocks of block-scale prefetch in the FP8 epilogue
@@ -160,8 +158,8 @@ struct alignas(16) Aux {
         float xch[4][2][16 * 32];                       // swapped SwiGLU exchange
     };
 };
-// The Aux block sits right after Shared; only kernels whose Geo::kAux is set
-// allocate it, and only their code paths reach it.
+// The Aux block sits right after Shared; every kernel but the pair store
+// kernel allocates it, and only the code paths of those kernels reach it.
 __device__ __forceinline__ Aux& aux(Shared& S) {
     return *reinterpret_cast<Aux*>(reinterpret_cast<uint8_t*>(&S) + sizeof(Shared));
 }
@@ -172,7 +170,8 @@ __device__ __forceinline__ const Aux& aux(const Shared& S) {
 template <bool PAIR, int EPI>
 constexpr size_t smem_bytes() {
     using G = Geo<PAIR, EPI>;
-    return 1024 + static_cast<size_t>(G::kStages) * G::kStageBytes + sizeof(Shared) + (G::kAux ? sizeof(Aux) : 0);
+    constexpr bool with_aux = !(PAIR && EPI == EPI_STORE);
+    return 1024 + static_cast<size_t>(G::kStages) * G::kStageBytes + sizeof(Shared) + (with_aux ? sizeof(Aux) : 0);
 }
 static_assert(smem_bytes<false, EPI_STORE>() <= 227 * 1024 && smem_bytes<false, EPI_SWIGLU_Q>() <= 227 * 1024 &&
                   smem_bytes<true, EPI_STORE>() <= 227 * 1024 && smem_bytes<true, EPI_SWIGLU>() <= 227 * 1024,
