@@ -24,22 +24,48 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// One warp per (row, 128-column group); lane l holds columns 4l .. 4l+3.
+// A half-warp per (row, 128-column group): lane l of the half holds columns
+// 8l .. 8l+7 (one 16-byte load), so a warp covers two groups at a time.  Each
+// warp walks its pairs of groups a grid-stride apart, kUnroll at a time with
+// all their loads issued first, so that enough bytes are in flight.  The
+// per-element IEEE divisions dominate the instruction count.
+constexpr int kUnroll = 4;
+
 __global__ void __launch_bounds__(256)
-act_quant_kernel(const uint2* __restrict__ x, int64_t M, int G, uint32_t* __restrict__ q,
+act_quant_kernel(const uint4* __restrict__ x, int64_t groups, uint2* __restrict__ q,
                  float* __restrict__ scales) {
-    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (gw >= M * G) return;
-    const uint2 v = __ldg(x + gw * 32 + lane);     // group gw = row * G + g, 256 bytes
-    const float a = moe::bf16_lo(v.x), b = moe::bf16_hi(v.x);
-    const float c = moe::bf16_lo(v.y), d = moe::bf16_hi(v.y);
-    float amax = fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(d)));
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    for (int64_t base = warp; base * 2 < groups; base += nwarps * kUnroll) {
+        uint4 v[kUnroll];
+        int64_t grp[kUnroll];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float s = fp8_scale(amax);
-    q[gw * 32 + lane] = quant4(a, b, c, d, s);
-    if (lane == 0) scales[gw] = s;
+        for (int u = 0; u < kUnroll; ++u) {       // group = 2 * pair + half, 256 bytes each
+            grp[u] = 2 * (base + u * nwarps) + half;
+            v[u] = grp[u] < groups ? __ldg(x + grp[u] * 16 + hl) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = moe::bf16_lo(w[i]);
+                f[2 * i + 1] = moe::bf16_hi(w[i]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const float sc = fp8_scale(amax);
+            if (grp[u] < groups) {
+                q[grp[u] * 16 + hl] = make_uint2(quant4(f[0], f[1], f[2], f[3], sc), quant4(f[4], f[5], f[6], f[7], sc));
+                if (hl == 0) scales[grp[u]] = sc;
+            }
+        }
+    }
 }
 
 // One CTA per (expert, 128-row block, 128-column block); thread t covers row
@@ -95,12 +121,15 @@ extern "C" moe_status_t moe_act_quant_fp8(const void* x, int M, int K, uint8_t* 
                                           moe_stream_t stream) {
     MOE_CHECK_ARG(x && q && scales && M >= 1 && K >= 128 && K % 128 == 0);
     MOE_CHECK_ARG(moe::aligned16(x) && moe::aligned16(q) && moe::aligned16(scales));
-    const int G = K / 128;
-    const int64_t warps = static_cast<int64_t>(M) * G;
+    const int64_t groups = static_cast<int64_t>(M) * (K / 128);
+    const int64_t pairs = (groups + 1) / 2;                      // a warp handles a pair at a time
+    // one pair per warp up to a full GPU of warps; beyond that each warp
+    // takes several pairs, kUnroll of them in flight
+    const int64_t cap = static_cast<int64_t>(moe::sm_count() > 0 ? moe::sm_count() : 148) * 64;
+    const int64_t warps = pairs < cap ? pairs : cap;
     const int64_t blocks = (warps + 7) / 8;
-    MOE_CHECK_ARG(blocks < INT32_MAX);
     act_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint2*>(x), M, G, reinterpret_cast<uint32_t*>(q), scales);
+        static_cast<const uint4*>(x), groups, reinterpret_cast<uint2*>(q), scales);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

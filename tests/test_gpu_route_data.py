@@ -121,6 +121,8 @@ def test_bad_expert_id_is_reported_not_placed(moe):
 def _act_inputs():
     g = np.random.default_rng(7)
     yield "normal", synth.dense_rows(333, 1024, 1)
+    yield "odd-groups", synth.dense_rows(3, 384, 5)          # 9 groups: one half-warp idles
+    yield "one-group", synth.dense_rows(1, 128, 6)
     heavy = g.standard_t(2, size=(64, 2048)).astype(np.float32) * 30
     heavy[3, :128] = 0                                       # an all-zero group
     heavy[4, 128:256] = 2.0 ** -100                          # subnormal codes only
