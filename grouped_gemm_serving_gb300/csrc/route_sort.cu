@@ -12,7 +12,7 @@
 //                       l' = logits + bias (ties to the lower id), softmax
 //                       weights, sentinel mask; then a warp-aggregated
 //                       (__match_any_sync) atomic histogram per sort block.
-//   2. route_scatter    one CTA per sort block of up to 2048 slots: global
+//   2. route_scatter    one CTA per sort block of up to 1024 slots: global
 //                       bin starts from the histograms (warp shuffle scan),
 //                       then a stable in-order rank of every slot from
 //                       per-warp match_any peer masks.  Writes sorted_rows,
@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxSlotsPerBlock = 2048;
+constexpr int kMaxSlotsPerBlock = 1024;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 32;
 
@@ -150,7 +150,7 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // warp w owns a contiguous run of at most 256 of the block's slots; its ids
+    // warp w owns a contiguous run of at most 128 of the block's slots; its ids
     // are loaded once, up front, so the loads overlap the count summation
     const int64_t blk0 = static_cast<int64_t>(b) * slots_per_block;
     const int64_t blk1 = blk0 + slots_per_block < R ? blk0 + slots_per_block : R;

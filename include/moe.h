@@ -149,9 +149,9 @@ moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
  * The per-sort-block histogram lives in a static device array of 256 KiB
  * inside libmoe.so (present on every GPU that loads the library, until the
  * process exits).  It holds blocks * (E + 1) 32-bit counters, where
- * blocks = ceil(T / floor(2048 / k)); a request that needs more returns
+ * blocks = ceil(T / floor(1024 / k)); a request that needs more returns
  * MOE_ERR_WORKSPACE with nothing enqueued (for example E = 256 allows up to
- * 255 blocks, about 522 thousand slots at k = 8).
+ * 255 blocks, about 261 thousand slots at k = 8).
  * The call allocates and frees nothing.  On its first call on a device it
  * looks up the array's device address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture.  Each call clears

@@ -60,9 +60,9 @@ def test_route_sort_bit_exact(moe, wl):
     _check_route(moe, wl)
 
 
-# Up to 2048 slots (T*k) form one sort block; one token more makes two.  Both
-# sides of the boundary, and a single token.
-@pytest.mark.parametrize("T", [1, 3, 511, 512, 513])
+# Up to 1024 slots (T*k) form one sort block; one token more makes two.  Both
+# sides of the one- and two-block boundaries, and a single token.
+@pytest.mark.parametrize("T", [1, 3, 255, 256, 257, 511, 512, 513])
 def test_route_sort_single_block_boundary(moe, T):
     _check_route(moe, synth.Workload(f"b{T}", T=T, E=16, k=4, H=8, I=8, n_sentinel=min(5, 4 * T - 1),
                                      bias="normal0.5"))
