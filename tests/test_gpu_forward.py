@@ -139,3 +139,24 @@ def test_expert_parallel_shards_on_one_gpu(moe):
     assert err.max() <= TOL["bf16"], err.max()
     dead = (ids == wl.E).all(axis=1)
     assert np.all(total[dead] == 0)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_forward_is_bit_reproducible(moe, fp8):
+    """Every result is the same, bit for bit, from run to run: no floating-point
+    atomics, fixed reduction orders.  Two runs of a layer with sentinels and a
+    skewed routing (several token tiles per expert) compare byte for byte."""
+    wl = synth.Workload("repro-16e-top4", T=1500, E=16, k=4, H=256, I=384, n_sentinel=60, bias="normal0.5")
+    x, logits, bias, mask = (synth.hidden_states(wl), synth.router_logits(wl), synth.expert_bias(wl),
+                             synth.sentinel_mask(wl))
+    W1, W2 = synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    if fp8:
+        (q1, s1), (q2, s2) = quantised_weights(moe, W1), quantised_weights(moe, W2)
+        args = (q1, q2, s1, s2)
+    else:
+        args = (dev_bf16(W1), dev_bf16(W2))
+    runs = [run_forward(moe, wl, x, *args, logits=logits, bias=bias, mask=mask) for _ in range(3)]
+    for y, ids, w in runs[1:]:
+        assert np.array_equal(y.view(np.uint32), runs[0][0].view(np.uint32))
+        assert np.array_equal(ids, runs[0][1])
+        assert np.array_equal(w.view(np.uint32), runs[0][2].view(np.uint32))

@@ -124,3 +124,20 @@ def test_full_size_gate_up_gradients_sampled(moe):
     pairs[-1] = [E - 1, N - 1]
     got = host_f32_from_bf16(dB)[pairs[:, 0], pairs[:, 1]]
     assert_close_bf16(got, oracle.grouped_gemm_wgrad_bf16(A, dC, off, E, pairs=pairs))
+
+
+def test_gradients_are_bit_reproducible(moe):
+    E, M_cap, live, N, K = 8, 1100, 1000, 512, 136
+    off, live, A, B, dC = _operands(E, M_cap, live, N, K, seed=17)
+    Ad, Bd, dCd, offd = dev_bf16(A), dev_bf16(B), dev_bf16(dC), dev(off)
+    n1 = moe.moe_grouped_gemm_dgrad_workspace_size(E, N, K)
+    n2 = moe.moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K)
+    outs = []
+    for _ in range(2):
+        dA = torch.empty((M_cap, K), dtype=torch.bfloat16, device="cuda")
+        dB = torch.empty((E, N, K), dtype=torch.bfloat16, device="cuda")
+        moe.moe_grouped_gemm_dgrad(dCd, Bd, offd, E, M_cap, N, K, dA, _ws(moe, n1), n1)
+        moe.moe_grouped_gemm_wgrad(Ad, dCd, offd, E, M_cap, N, K, dB, _ws(moe, n2), n2)
+        assert moe.moe_get_device_error() == 0
+        outs.append((host_bf16_bits(dA), host_bf16_bits(dB)))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
