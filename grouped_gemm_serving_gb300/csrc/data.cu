@@ -22,11 +22,11 @@ __device__ __forceinline__ int live_rows(const int32_t* offsets, int E, int M_ca
     return L;
 }
 
-// xp[p] = x[sorted_rows[p] / k] for p < L; one warp per (row, segment),
-// persistent over them.  row_vecs = bytes per row / 16; a row is split into
-// segs segments of seg_vecs vectors (segs = 1 unless there are too few rows
-// to fill the GPU).  FP8 rows also move their group scales into the
-// group-major layout xp_scales[g * M_cap + p].
+// xp[p] = x[sorted_rows[p] / k] for p < L; one warp per (row, segment)
+// (the loop also covers a smaller grid).  row_vecs = bytes per row / 16; a
+// row is split into segs segments of seg_vecs vectors (segs = 1 unless there
+// are too few rows to fill the GPU).  FP8 rows also move their group scales
+// into the group-major layout xp_scales[g * M_cap + p].
 __global__ void __launch_bounds__(kThreads)
 permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, int T, int k,
                int row_vecs, int segs, int seg_vecs, int G, const int32_t* __restrict__ sorted_rows,
@@ -115,18 +115,21 @@ combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
         }
     }
     uint4* dst = out + static_cast<int64_t>(t) * row_vecs;
-    // The trip counts are the same for every lane, so the shuffles see a full
-    // warp.  Up to eight slots' vectors are loaded before any is used, so they
-    // are in flight together; they are then accumulated in slot order.
+    // Two 32-vector chunks per pass.  The trip counts are the same for every
+    // lane, so the shuffles see a full warp.  Up to eight slots' vectors of
+    // both chunks are loaded before any is used, so they are in flight
+    // together; they are then accumulated in slot order.
     constexpr int KG = 8;
-    for (int c0 = 0; c0 < row_vecs; c0 += 32) {
-        const int c = c0 + lane;
-        const bool in_row = c < row_vecs;
-        float acc[8];
+    for (int c0 = 0; c0 < row_vecs; c0 += 64) {
+        const int ca = c0 + lane, cb = c0 + 32 + lane;
+        const bool ina = ca < row_vecs, inb = cb < row_vecs;
+        float acc[2][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
         for (int j0 = 0; j0 < k; j0 += KG) {
-            uint4 v[KG];
+            uint4 va[KG], vb[KG];
             float wj[KG];
             bool use[KG];
 #pragma unroll
@@ -134,23 +137,31 @@ combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
                 const int j = j0 + g;
                 const int row = __shfl_sync(0xffffffffu, my_row, j & 31);
                 wj[g] = __shfl_sync(0xffffffffu, my_w, j & 31);
-                use[g] = j < k && row >= 0 && in_row;   // sentinel slots are skipped
-                v[g] = use[g] ? __ldg(Y2 + static_cast<int64_t>(row) * row_vecs + c) : make_uint4(0, 0, 0, 0);
+                use[g] = j < k && row >= 0;   // sentinel slots are skipped
+                const uint4* src = Y2 + static_cast<int64_t>(row) * row_vecs;
+                va[g] = use[g] && ina ? __ldg(src + ca) : make_uint4(0, 0, 0, 0);
+                vb[g] = use[g] && inb ? __ldg(src + cb) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int g = 0; g < KG; ++g) {
                 if (!use[g]) continue;
-                const uint32_t vs[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+                const uint32_t a4[4] = {va[g].x, va[g].y, va[g].z, va[g].w};
+                const uint32_t b4[4] = {vb[g].x, vb[g].y, vb[g].z, vb[g].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = fmaf(wj[g], moe::bf16_lo(vs[i]), acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(wj[g], moe::bf16_hi(vs[i]), acc[2 * i + 1]);
+                    acc[0][2 * i] = fmaf(wj[g], moe::bf16_lo(a4[i]), acc[0][2 * i]);
+                    acc[0][2 * i + 1] = fmaf(wj[g], moe::bf16_hi(a4[i]), acc[0][2 * i + 1]);
+                    acc[1][2 * i] = fmaf(wj[g], moe::bf16_lo(b4[i]), acc[1][2 * i]);
+                    acc[1][2 * i + 1] = fmaf(wj[g], moe::bf16_hi(b4[i]), acc[1][2 * i + 1]);
                 }
             }
         }
-        if (in_row)
-            dst[c] = make_uint4(moe::pack_bf16x2(acc[0], acc[1]), moe::pack_bf16x2(acc[2], acc[3]),
-                                moe::pack_bf16x2(acc[4], acc[5]), moe::pack_bf16x2(acc[6], acc[7]));
+        if (ina)
+            dst[ca] = make_uint4(moe::pack_bf16x2(acc[0][0], acc[0][1]), moe::pack_bf16x2(acc[0][2], acc[0][3]),
+                                 moe::pack_bf16x2(acc[0][4], acc[0][5]), moe::pack_bf16x2(acc[0][6], acc[0][7]));
+        if (inb)
+            dst[cb] = make_uint4(moe::pack_bf16x2(acc[1][0], acc[1][1]), moe::pack_bf16x2(acc[1][2], acc[1][3]),
+                                 moe::pack_bf16x2(acc[1][4], acc[1][5]), moe::pack_bf16x2(acc[1][6], acc[1][7]));
     }
 }
 
@@ -273,7 +284,11 @@ extern "C" moe_status_t moe_permute(moe_dtype_t dtype, const void* x, const floa
     const int64_t want = M_cap < sm * kWarpsPerBlock ? (static_cast<int64_t>(sm) * 32 + M_cap - 1) / M_cap : 1;
     const int segs = static_cast<int>(want < max_segs ? (want > 1 ? want : 1) : max_segs);
     const int seg_vecs = ((row_vecs + segs - 1) / segs + 31) / 32 * 32;
-    permute_kernel<<<persistent_blocks(static_cast<int64_t>(M_cap) * segs), kThreads, 0,
+    // one warp per (row, segment): the block scheduler balances the rows,
+    // where a grid capped at a few blocks per SM dealt them out unevenly
+    const int64_t units = static_cast<int64_t>(M_cap) * segs;
+    MOE_CHECK_ARG((units + kWarpsPerBlock - 1) / kWarpsPerBlock < INT_MAX);
+    permute_kernel<<<static_cast<int>((units + kWarpsPerBlock - 1) / kWarpsPerBlock), kThreads, 0,
                      reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(x), fp8 ? x_scales : nullptr, T, k, row_vecs, segs, seg_vecs, G, sorted_rows,
         offsets, E, M_cap, static_cast<uint4*>(xp), fp8 ? xp_scales : nullptr, err);
