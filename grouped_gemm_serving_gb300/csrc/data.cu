@@ -91,7 +91,12 @@ swiglu_kernel(const uint4* __restrict__ Y1, const int32_t* __restrict__ offsets,
 
 // out[t] = sum_j w[t,j] * Y2[row_pos[t*k+j]] over non-sentinel slots, fp32 in
 // j order; one warp per token, 8 columns (one 16-byte vector) per lane step.
-__global__ void __launch_bounds__(kThreads)
+// KG slots are loaded at a time.  With KG = 4 (top-k up to 4) the kernel
+// fits 64 registers, so four blocks share an SM: a 4096-token grid then runs
+// in one wave with 32 warps per SM, where KG = 8 (114 registers) allows two
+// blocks and left the second wave two-thirds full.
+template <int KG, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
                const float* __restrict__ w, const int32_t* __restrict__ row_pos, int T, int k,
                int row_vecs, int E, int64_t M_cap, uint4* __restrict__ out, int* err) {
@@ -116,10 +121,9 @@ combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
     }
     uint4* dst = out + static_cast<int64_t>(t) * row_vecs;
     // Two 32-vector chunks per pass.  The trip counts are the same for every
-    // lane, so the shuffles see a full warp.  Up to eight slots' vectors of
-    // both chunks are loaded before any is used, so they are in flight
-    // together; they are then accumulated in slot order.
-    constexpr int KG = 8;
+    // lane, so the shuffles see a full warp.  Up to KG slots' vectors of both
+    // chunks are loaded before any is used, so they are in flight together;
+    // they are then accumulated in slot order.
     for (int c0 = 0; c0 < row_vecs; c0 += 64) {
         const int ca = c0 + lane, cb = c0 + 32 + lane;
         const bool ina = ca < row_vecs, inb = cb < row_vecs;
@@ -321,7 +325,8 @@ extern "C" moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, con
     const int sm = moe::sm_count() > 0 ? moe::sm_count() : 148;
     if (T >= sm * kWarpsPerBlock) {   // at least a block of tokens per SM: one warp per token
         const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-        combine_kernel<<<blocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        auto kern = k <= 4 ? combine_kernel<4, 4> : combine_kernel<8, 1>;
+        kern<<<blocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
             static_cast<const uint4*>(Y2), topk_ids, topk_w, row_pos, T, k, H / 8, E,
             static_cast<int64_t>(T) * k, static_cast<uint4*>(out), err);
         MOE_CHECK_LAUNCH();

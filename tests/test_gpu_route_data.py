@@ -194,7 +194,13 @@ def test_permute_fp8_bytes_and_scales(moe):
     assert np.array_equal(host(xs).T[:L], xs_ref[:L])
 
 
-@pytest.mark.parametrize("T,E,k,H,n_sent", [(64, 8, 2, 128, 8), (700, 32, 4, 2880, 90), (300, 128, 8, 2048, 0)])
+# The first three take the row-split path (few tokens); the rest have a block
+# of tokens per SM and take one warp per token, in both of its slot-group
+# sizes (top-k up to 4, and above), with ragged row lengths.
+@pytest.mark.parametrize("T,E,k,H,n_sent", [(64, 8, 2, 128, 8), (700, 32, 4, 2880, 90), (300, 128, 8, 2048, 0),
+                                            (1300, 16, 1, 264, 50), (1300, 16, 3, 1032, 100),
+                                            (1400, 64, 4, 2880, 200), (1300, 64, 5, 520, 0),
+                                            (1250, 128, 8, 264, 300)])
 def test_combine_matches_oracle(moe, T, E, k, H, n_sent):
     ids, w, sr, rp, off = _routing(T, E, k, n_sent, 5)
     R = T * k
@@ -211,8 +217,9 @@ def test_combine_matches_oracle(moe, T, E, k, H, n_sent):
     assert np.all(got[dead] == 0)
 
 
-def test_permute_then_combine_is_identity(moe):
-    T, E, k, H = 400, 16, 4, 512
+@pytest.mark.parametrize("T,k", [(400, 4), (1300, 1), (1300, 2), (1300, 4), (1300, 8)])
+def test_permute_then_combine_is_identity(moe, T, k):
+    E, H = 16, 512
     ids, _, sr, rp, off = _routing(T, E, k, 0, 9)
     x = synth.dense_rows(T, H, 10)
     xp = torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda")
