@@ -172,7 +172,7 @@ combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,
 // The same sum for small T, with several warps per token so that the grid
 // still fills the GPU: warp w handles token w / segs, vectors
 // [seg * seg_vecs, ...) of its row.  Same arithmetic and order per element.
-constexpr int kCombineChunks = 1;
+constexpr int kCombineChunks = 1;   // 32-vector chunks a warp loads per pass
 
 __global__ void __launch_bounds__(kThreads)
 combine_split_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ ids,

@@ -104,7 +104,6 @@ constexpr int kGatherWarps = 3; // warps 0, 2, 3 issue the row gathers of gather
 constexpr int BT = 256;
 constexpr int kSwapFeatSwiglu = 128;  // h features per pair tile (each CTA: 64 gate + 64 up rows)
 constexpr int kSwapFeatStore = 256;   // output features per pair tile (128 per CTA)
-constexpr bool kSwapBf16 = true;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr int kRegsLow = 56, kRegsHigh = 224;
@@ -1104,7 +1103,7 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     const int half = swiglu ? N / 2 : 0;
     // bf16 without a gather runs with swapped operands: weight-row tiles x
     // token tiles of up to BT rows
-    const bool swap = kSwapBf16 && !fp8 && !gx;
+    const bool swap = !fp8 && !gx;
     const int feat = swap ? (swiglu ? kSwapFeatSwiglu : kSwapFeatStore) : (swiglu ? BN / 2 : BN);
     const int n_tiles = ((swiglu ? half : N) + feat - 1) / feat;
     const int64_t max_tiles = (static_cast<int64_t>(M_cap) / (swap ? BT : BM) + E) * n_tiles;
