@@ -26,7 +26,10 @@ __device__ __forceinline__ int live_rows(const int32_t* offsets, int E, int M_ca
 // (the loop also covers a smaller grid).  row_vecs = bytes per row / 16; a
 // row is split into segs segments of seg_vecs vectors (segs = 1 unless there
 // are too few rows to fill the GPU).  FP8 rows also move their group scales
-// into the group-major layout xp_scales[g * M_cap + p].
+// into the group-major layout xp_scales[g * M_cap + p]: the warp of every
+// eighth row (segment 0) moves the scales of rows p .. p+7, so that a group's
+// eight values fill one 32-byte sector instead of eight rows each scattering
+// a value over every group's line.
 __global__ void __launch_bounds__(kThreads)
 permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, int T, int k,
                int row_vecs, int segs, int seg_vecs, int G, const int32_t* __restrict__ sorted_rows,
@@ -41,6 +44,19 @@ permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, 
     for (int64_t w = warp0; w < n; w += nwarps) {
         const int p = static_cast<int>(w / segs);
         const int seg = static_cast<int>(w - static_cast<int64_t>(p) * segs);
+        if (x_scales && seg == 0 && (p & 7) == 0) {
+            // lane l: row p + l % 8, groups l / 8, l / 8 + 4, ...; a row
+            // with a bad slot is skipped here and reported by its own warp
+            const int pr = p + (lane & 7);
+            int tr = -1;
+            if (pr < L) {
+                const int sr = sorted_rows[pr];
+                if (sr >= 0 && sr / k < T) tr = sr / k;
+            }
+            if (tr >= 0)
+                for (int g = lane >> 3; g < G; g += 4)
+                    xp_scales[static_cast<int64_t>(g) * M_cap + pr] = __ldg(x_scales + static_cast<int64_t>(tr) * G + g);
+        }
         const int slot = sorted_rows[p];
         const int t = slot / k;
         if (slot < 0 || t >= T) {
@@ -52,9 +68,6 @@ permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, 
         const int v_end = min(row_vecs, (seg + 1) * seg_vecs);
 #pragma unroll 8
         for (int i = seg * seg_vecs + lane; i < v_end; i += 32) dst[i] = __ldg(src + i);
-        if (x_scales && seg == 0)
-            for (int g = lane; g < G; g += 32)
-                xp_scales[static_cast<int64_t>(g) * M_cap + p] = __ldg(x_scales + static_cast<int64_t>(t) * G + g);
     }
 }
 
