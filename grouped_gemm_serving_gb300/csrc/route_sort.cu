@@ -9,7 +9,8 @@
 //
 // Kernels (one stream, no host synchronisation):
 //   1. route_topk_hist  one warp per token: k rounds of warp arg-max over
-//                       l' = logits + bias (ties to the lower id), softmax
+//                       l' = logits + bias (ties to the lower id; two warp
+//                       reductions per round on order-preserving keys), softmax
 //                       weights, sentinel mask; then a warp-aggregated
 //                       (__match_any_sync) atomic histogram per sort block.
 //   2. route_scatter    one CTA per sort block of up to 1024 slots: global
@@ -45,8 +46,16 @@ SortGeometry geometry(int T, int k) {
     return g;
 }
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
+// Order-preserving map of a float to an unsigned key: a larger float gives a
+// larger key and +0 and -0 the same key.  NaN maps to 0, below every number,
+// so it is never picked; 0 also marks a logit already picked.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);   // -0 + 0 = +0
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // Ids outside [0, E] cannot be placed: they are sorted as sentinels and the
@@ -83,24 +92,26 @@ route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias
                 v[j] = -INFINITY;
             }
         }
-        uint32_t taken = 0;
+        // each pick: the largest key over the warp (one warp reduction), then
+        // the lowest expert id holding it (a second one); a lane's candidate
+        // is its first slot with its largest key, the lowest id of the lane
+        uint32_t key[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) key[j] = lane + 32 * j < E ? order_key(v[j]) : 0u;
+        uint32_t taken = 0;   // bit j: this lane's slot j was picked
         float my_v = -INFINITY;
         for (int r = 0; r < k; ++r) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
+            uint32_t bk = 0u;
+            int bj = 0;
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                const int e = lane + 32 * j;
-                if (!((taken >> j) & 1u) && better(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
+                const uint32_t kj = (taken >> j) & 1u ? 0u : key[j];
+                if (kj > bk) { bk = kj; bj = j; }
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == r) { my_v = bv; my_id = bi; }
+            const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+            const int bi = __reduce_min_sync(0xffffffffu, m != 0u && bk == m ? lane + 32 * bj : INT_MAX);
+            if (m != 0u && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == r) { my_v = m != 0u ? key_value(m) : -INFINITY; my_id = bi; }
         }
         const float mx = __shfl_sync(0xffffffffu, my_v, 0);  // pick 0 is the maximum
         float part = 0.0f;
@@ -168,7 +179,18 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
     // 1. per bin: total over all blocks and the count in blocks before this one
     for (int bin = threadIdx.x; bin < nb; bin += kThreads) {
         int all = 0, before = 0;
-        for (int bb = 0; bb < nblocks; ++bb) {
+        int bb = 0;
+        for (; bb + 16 <= nblocks; bb += 16) {   // sixteen independent loads in flight
+            int c[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) c[i] = counts[(bb + i) * nb + bin];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                all += c[i];
+                before += bb + i < b ? c[i] : 0;
+            }
+        }
+        for (; bb < nblocks; ++bb) {
             const int c = counts[bb * nb + bin];
             all += c;
             before += bb < b ? c : 0;
