@@ -117,6 +117,9 @@ moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream);
  *              j-th pick, and topk_w[t, j] = softmax over the k picks
  *              (renormalize != 0) or the full softmax over E evaluated at the
  *              pick (renormalize == 0).  topk_ids/topk_w are then outputs.
+ *              -0 and +0 tie.  A NaN l' is never picked: a token with fewer
+ *              than k other values gets an invalid pick, which is recorded as
+ *              MOE_DEVERR_ROUTE and sorted as a sentinel.
  *              When NULL, topk_ids is an input (ids in [0, E]; E = sentinel)
  *              and topk_w is not touched (may be NULL).
  * expert_bias  fp32 [E] or NULL.
