@@ -30,7 +30,7 @@ __device__ __forceinline__ int live_rows(const int32_t* offsets, int E, int M_ca
 // eighth row (segment 0) moves the scales of rows p .. p+7, so that a group's
 // eight values fill one 32-byte sector instead of eight rows each scattering
 // a value over every group's line.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)   // 32 registers: 64 warps per SM
 permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, int T, int k,
                int row_vecs, int segs, int seg_vecs, int G, const int32_t* __restrict__ sorted_rows,
                const int32_t* __restrict__ offsets, int E, int M_cap, uint4* __restrict__ xp,
@@ -66,7 +66,7 @@ permute_kernel(const uint4* __restrict__ x, const float* __restrict__ x_scales, 
         const uint4* src = x + static_cast<int64_t>(t) * row_vecs;
         uint4* dst = xp + static_cast<int64_t>(p) * row_vecs;
         const int v_end = min(row_vecs, (seg + 1) * seg_vecs);
-#pragma unroll 8
+#pragma unroll 4
         for (int i = seg * seg_vecs + lane; i < v_end; i += 32) dst[i] = __ldg(src + i);
     }
 }

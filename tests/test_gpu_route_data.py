@@ -117,6 +117,35 @@ def test_bad_expert_id_is_reported_not_placed(moe):
     assert host(r["offsets"])[-1] == 127                     # the bad slot sorts as a sentinel
 
 
+def test_route_never_picks_nan(moe):
+    """A NaN logit is never picked; with at least k other values per token the
+    picks and weights are those of the oracle with the NaNs at -inf."""
+    g = np.random.default_rng(8)
+    T, E, k = 300, 40, 4
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    nan = g.random((T, E)) < 0.4
+    nan[:, 5:5 + k] = False                                  # k finite values per token at least
+    logits[nan] = np.nan
+    ids, w = oracle.route_topk(np.where(nan, -np.inf, logits).astype(np.float32), None, k)
+    r = moe.route_sort_t(E, k, logits=dev(logits))
+    _no_device_error(moe)
+    assert np.array_equal(host(r["ids"]), ids)
+    np.testing.assert_allclose(host(r["w"]), w, rtol=2e-6)
+
+
+def test_route_too_few_numbers_is_reported(moe):
+    """A token with fewer than k non-NaN logits cannot be routed: the error is
+    recorded and its unfilled slots sort as sentinels."""
+    T, E, k = 64, 16, 4
+    logits = np.random.default_rng(9).standard_normal((T, E)).astype(np.float32)
+    logits[7, 2:] = np.nan                                   # two numbers for four picks
+    r = moe.route_sort_t(E, k, logits=dev(logits))
+    assert moe.moe_get_device_error() == moe.MOE_DEVERR_ROUTE
+    assert np.array_equal(np.sort(host(r["sorted_rows"])), np.arange(T * k))
+    assert host(r["offsets"])[-1] == T * k - 2
+    assert set(host(r["ids"])[7, :2]) == {0, 1}
+
+
 # ---------------------------------------------------------------- FP8 quantisation
 def _act_inputs():
     g = np.random.default_rng(7)
