@@ -68,14 +68,15 @@ __device__ __forceinline__ int checked_id(int id, int E, int* err) {
     return id;
 }
 
+// Routes token t on one warp: the k picks (or the given ids), the weights
+// and the sentinel mask, written to ids/w.  Returns, in lane j < k, the
+// checked id of slot j (a bad id is reported and returned as E).
 template <int NV>   // logits per lane: E <= 32 * NV
-__global__ void __launch_bounds__(kThreads)
-route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias,
-                const uint8_t* __restrict__ mask, int32_t* ids, float* __restrict__ w, int T,
-                int E, int k, int renormalize, int slots_per_block, int* counts, int* err) {
+__device__ __forceinline__ int route_token(const float* __restrict__ logits, const float* __restrict__ bias,
+                                           const uint8_t* __restrict__ mask, int32_t* ids,
+                                           float* __restrict__ w, int t, int E, int k, int renormalize,
+                                           int* err) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (t >= T) return;
     const int64_t slot0 = static_cast<int64_t>(t) * k;
     int my_id = E;  // lane j < k: the id of slot j
 
@@ -137,6 +138,19 @@ route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias
         }
     }
     if (lane < k) my_id = checked_id(my_id, E, err);
+    return my_id;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kThreads)
+route_topk_hist(const float* __restrict__ logits, const float* __restrict__ bias,
+                const uint8_t* __restrict__ mask, int32_t* ids, float* __restrict__ w, int T,
+                int E, int k, int renormalize, int slots_per_block, int* counts, int* err) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int64_t slot0 = static_cast<int64_t>(t) * k;
+    const int my_id = route_token<NV>(logits, bias, mask, ids, w, t, E, k, renormalize, err);
 
     // histogram of this token's slots into its sort block, one atomic per
     // distinct id in the warp
@@ -274,6 +288,108 @@ route_scatter(const int32_t* ids, int64_t R, int E, int slots_per_block, int nbl
     }
 }
 
+// A batch whose slots form a single sort block (T * k <= 1024) and whose
+// tokens are few: one CTA of 32 warps routes the tokens (warp w takes tokens
+// w, w + 32, ...), then sorts the slots in shared memory.  It replaces the
+// histogram memset and the second launch of the two-kernel path, which cost
+// more than the work itself at decode batch sizes (64 tokens, 32 experts:
+// 10.2 against 13.3 us) -- as long as each warp routes few tokens of few
+// logits: 128 tokens of 256 experts took 28.7 us against 17.4.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+
+template <int NV>
+__global__ void __launch_bounds__(kSmallThreads)
+route_small(const float* __restrict__ logits, const float* __restrict__ bias,
+            const uint8_t* __restrict__ mask, int32_t* ids, float* __restrict__ w, int T, int E, int k,
+            int renormalize, int32_t* __restrict__ sorted_rows, int32_t* __restrict__ row_pos,
+            int32_t* __restrict__ offsets, int* err) {
+    __shared__ int sid[kMaxSlotsPerBlock];
+    __shared__ int whist[kSmallWarps][kMaxE + 1];
+    __shared__ int bin_start[kMaxE + 1];
+    __shared__ int bin_total[kMaxE + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = E + 1;
+    const int R = T * k;
+    for (int i = threadIdx.x; i < kSmallWarps * nb; i += kSmallThreads) whist[i / nb][i % nb] = 0;
+    for (int t = warp; t < T; t += kSmallWarps) {
+        const int id = route_token<NV>(logits, bias, mask, ids, w, t, E, k, renormalize, err);
+        if (lane < k) sid[t * k + lane] = id;
+    }
+    __syncthreads();
+
+    // slot s = threadIdx.x: per-warp histograms, then for every bin the
+    // exclusive prefix over warps and the total
+    const int s = threadIdx.x;
+    const int id = s < R ? sid[s] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, id);
+    if (id >= 0 && lane == __ffs(peers) - 1) whist[warp][id] = __popc(peers);
+    __syncthreads();
+    for (int bin = threadIdx.x; bin < nb; bin += kSmallThreads) {
+        int acc = 0;
+        for (int wi = 0; wi < kSmallWarps; ++wi) {
+            const int c = whist[wi][bin];
+            whist[wi][bin] = acc;
+            acc += c;
+        }
+        bin_total[bin] = acc;
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive scan of the totals over bins
+        constexpr int PER = (kMaxE + 1 + 31) / 32;
+        int tot[PER];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int bin = lane * PER + i;
+            tot[i] = bin < nb ? bin_total[bin] : 0;
+            sum += tot[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int bin = lane * PER + i;
+            if (bin < nb) {
+                bin_start[bin] = run;
+                offsets[bin] = run;   // offsets[E] = live rows
+                run += tot[i];
+            }
+        }
+    }
+    __syncthreads();
+    if (id >= 0) {
+        const int pos = bin_start[id] + whist[warp][id] + __popc(peers & ((1u << lane) - 1u));
+        sorted_rows[pos] = s;
+        row_pos[s] = pos;
+    }
+}
+
+// Whether the single-CTA path takes this batch: one sort block, and at most
+// four (tokens per warp) x (logits per lane) of routing work per warp.
+bool use_small(int T, int E, int k) {
+    const int nv = E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8;
+    return static_cast<int64_t>(T) * k <= kMaxSlotsPerBlock && (T + kSmallWarps - 1) / kSmallWarps * nv <= 4;
+}
+
+void launch_small(cudaStream_t s, const float* logits, const float* bias, const uint8_t* mask, int32_t* ids,
+                  float* w, int T, int E, int k, int renormalize, int32_t* sorted_rows, int32_t* row_pos,
+                  int32_t* offsets, int* err) {
+    if (E <= 32)
+        route_small<1><<<1, kSmallThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, sorted_rows, row_pos, offsets, err);
+    else if (E <= 64)
+        route_small<2><<<1, kSmallThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, sorted_rows, row_pos, offsets, err);
+    else if (E <= 128)
+        route_small<4><<<1, kSmallThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, sorted_rows, row_pos, offsets, err);
+    else
+        route_small<8><<<1, kSmallThreads, 0, s>>>(logits, bias, mask, ids, w, T, E, k, renormalize, sorted_rows, row_pos, offsets, err);
+}
+
 void launch_topk_hist(cudaStream_t s, const float* logits, const float* bias, const uint8_t* mask,
                       int32_t* ids, float* w, int T, int E, int k, int renormalize,
                       int slots_per_block, int* counts, int* err) {
@@ -316,6 +432,12 @@ extern "C" moe_status_t moe_route_sort(const float* logits, const float* expert_
     if (!err) return MOE_ERR_CUDA;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (use_small(T, E, k)) {
+        launch_small(s, logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
+                     renormalize, sorted_rows, row_pos, offsets, err);
+        MOE_CHECK_LAUNCH();
+        return MOE_OK;
+    }
     const SortGeometry g = geometry(T, k);
     int* counts = static_cast<int*>(ws);
     MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(g.blocks) * (E + 1) * sizeof(int), s));
@@ -379,12 +501,18 @@ extern "C" moe_status_t moe_route_sort_noalloc(const float* logits, const float*
     const SortGeometry g = geometry(T, k);
     const size_t ints = static_cast<size_t>(g.blocks) * (E + 1);
     if (ints > kStaticScratchInts) return MOE_ERR_WORKSPACE;   // beyond the static scratch
-    int* counts = static_scratch();
-    if (!counts) return MOE_ERR_CUDA;
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
-
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (use_small(T, E, k)) {
+        launch_small(s, logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
+                     renormalize, sorted_rows, row_pos, offsets, err);
+        MOE_CHECK_LAUNCH();
+        return MOE_OK;
+    }
+    int* counts = static_scratch();
+    if (!counts) return MOE_ERR_CUDA;
+
     MOE_CHECK_CUDA(cudaMemsetAsync(counts, 0, ints * sizeof(int), s));
     launch_topk_hist(s, logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E,
                      k, renormalize, g.slots_per_block, counts, err);

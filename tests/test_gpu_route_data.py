@@ -68,9 +68,20 @@ def test_route_sort_single_block_boundary(moe, T):
                                      bias="normal0.5"))
 
 
-def test_route_ties_go_to_lower_expert(moe):
+# A batch whose slots fit one sort block and whose routing work is small
+# (tokens per warp x logits per lane <= 4) is routed and sorted by a single
+# CTA: both sides of that limit for each logits-per-lane count.
+@pytest.mark.parametrize("T,E,k", [(128, 32, 8), (129, 32, 4), (128, 8, 8), (64, 64, 8), (65, 64, 2),
+                                   (32, 128, 8), (33, 128, 4), (1, 256, 8), (100, 200, 3)])
+def test_route_sort_single_cta_boundary(moe, T, E, k):
+    _check_route(moe, synth.Workload(f"c{T}-{E}-{k}", T=T, E=E, k=k, H=8, I=8, n_sentinel=min(7, T * k - 1),
+                                     bias="normal0.5"))
+
+
+@pytest.mark.parametrize("T", [500, 100])   # two-kernel and single-CTA paths
+def test_route_ties_go_to_lower_expert(moe, T):
     g = np.random.default_rng(3)
-    logits = g.integers(-1, 2, size=(500, 24)).astype(np.float32)   # heavy ties
+    logits = g.integers(-1, 2, size=(T, 24)).astype(np.float32)   # heavy ties
     ids, w = oracle.route_topk(logits, None, 5)
     r = moe.route_sort_t(24, 5, logits=dev(logits))
     assert np.array_equal(host(r["ids"]), ids)
