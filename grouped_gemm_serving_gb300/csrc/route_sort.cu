@@ -18,6 +18,9 @@
 //                       then a stable in-order rank of every slot from
 //                       per-warp match_any peer masks.  Writes sorted_rows,
 //                       row_pos and (block 0) offsets.
+// A small batch (one sort block, little routing work) instead runs
+//   route_small         one CTA of 32 warps: the same per-token routing, then
+//                       the sort of its <= 1024 slots in shared memory.
 #include <atomic>
 #include <climits>
 #include <mutex>
