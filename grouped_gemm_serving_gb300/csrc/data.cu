@@ -106,7 +106,7 @@ swiglu_kernel(const uint4* __restrict__ Y1, const int32_t* __restrict__ offsets,
 // j order; one warp per token, 8 columns (one 16-byte vector) per lane step.
 // KG slots are loaded at a time.  With KG = 4 (top-k up to 4) the kernel
 // fits 64 registers, so four blocks share an SM: a 4096-token grid then runs
-// in one wave with 32 warps per SM, where KG = 8 (114 registers) allows two
+// in one wave with 32 warps per SM, where KG = 8 (118 registers) allows two
 // blocks and left the second wave two-thirds full.
 template <int KG, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
