@@ -209,7 +209,13 @@ class Step:
         self.times = {n: [] for n in self.names}
 
     def launches_per_step(self):
-        return len(self.names) + 1   # route_sort runs two kernels
+        # route_sort runs two kernels, or one for a small batch: a single sort
+        # block (T*k <= 1024) with at most four (tokens per warp) x (logits
+        # per lane) of routing work, the library's rule
+        T, E, k = self.wl.T, self.wl.E, self.wl.k
+        nv = 1 if E <= 32 else 2 if E <= 64 else 4 if E <= 128 else 8
+        route = 1 if T * k <= 1024 and -(-T // 32) * nv <= 4 else 2
+        return len(self.names) - 1 + route
 
     def run(self, record=False):
         wl, L, moe = self.wl, self.L, self.moe
