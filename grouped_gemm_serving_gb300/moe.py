@@ -84,9 +84,14 @@ def lib() -> C.CDLL:
     return _lib
 
 
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
 def status_string(status: int) -> str:
+    """moe_status_string for error messages: never raises."""
     try:
-        return lib().moe_status_string(status).decode()
+        return moe_status_string(status)
     except Exception:  # noqa: BLE001 - used while reporting another error
         return "unknown"
 

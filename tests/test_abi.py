@@ -32,13 +32,13 @@ def test_every_declared_symbol_is_exported(moe):
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
     # the binding wraps every declared entry point under the same name
-    assert all(hasattr(moe, n) or n == "moe_status_string" for n in names)
+    assert all(hasattr(moe, n) for n in names)
 
 
 def test_abi_version_and_status_strings(moe):
     assert moe.moe_abi_version() == 1
     for st in range(7):
-        assert moe.status_string(st) not in ("", "unknown status")
+        assert moe.moe_status_string(st) not in ("", "unknown status")
 
 
 def test_workspace_sizes(moe):
