@@ -142,7 +142,7 @@ moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
 
 /*
  * moe_route_sort_noalloc -- moe_route_sort without caller workspace.  The
- * paper has no counterpart: this entry point exists for callers that
+ * sources have no counterpart: this entry point exists for callers that
  * cannot allocate device memory themselves, such as a plug-in running inside
  * a serving engine that reserves and owns the whole device memory pool, or a
  * latency-critical path where an allocation call (which may synchronise the
