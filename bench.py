@@ -66,6 +66,14 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def route_kernels(T: int, E: int, k: int) -> int:
+    """Kernels moe_route_sort launches: two, or one for a small batch -- a
+    single sort block (T*k <= 1024) with at most four (tokens per warp) x
+    (logits per lane) of routing work, the library's rule."""
+    nv = 1 if E <= 32 else 2 if E <= 64 else 4 if E <= 128 else 8
+    return 1 if T * k <= 1024 and -(-T // 32) * nv <= 4 else 2
+
+
 class ClockSampler:
     """nvidia-smi sampled every 200 ms while the timed region runs."""
 
@@ -209,13 +217,7 @@ class Step:
         self.times = {n: [] for n in self.names}
 
     def launches_per_step(self):
-        # route_sort runs two kernels, or one for a small batch: a single sort
-        # block (T*k <= 1024) with at most four (tokens per warp) x (logits
-        # per lane) of routing work, the library's rule
-        T, E, k = self.wl.T, self.wl.E, self.wl.k
-        nv = 1 if E <= 32 else 2 if E <= 64 else 4 if E <= 128 else 8
-        route = 1 if T * k <= 1024 and -(-T // 32) * nv <= 4 else 2
-        return len(self.names) - 1 + route
+        return len(self.names) - 1 + route_kernels(self.wl.T, self.wl.E, self.wl.k)
 
     def run(self, record=False):
         wl, L, moe = self.wl, self.L, self.moe

@@ -25,3 +25,14 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_route_kernel_count_follows_the_library_rule():
+    """bench.py counts one routing kernel for the batches the library routes in
+    a single CTA (the boundaries the GPU routing tests exercise), two otherwise."""
+    sys.path.insert(0, ROOT)
+    import bench
+    one = [(64, 32, 4), (128, 32, 8), (128, 8, 8), (64, 64, 8), (32, 128, 8), (1, 32, 1)]
+    two = [(4096, 32, 4), (129, 32, 4), (65, 64, 2), (33, 128, 4), (1, 256, 8), (64, 256, 8), (200, 16, 8)]
+    assert all(bench.route_kernels(*a) == 1 for a in one)
+    assert all(bench.route_kernels(*a) == 2 for a in two)
