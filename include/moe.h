@@ -155,10 +155,12 @@ moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
  * blocks = ceil(T / floor(1024 / k)); a request that needs more returns
  * MOE_ERR_WORKSPACE with nothing enqueued (for example E = 256 allows up to
  * 255 blocks, about 261 thousand slots at k = 8).
- * The call allocates and frees nothing.  On its first call on a device it
- * looks up the array's device address (cudaGetSymbolAddress, with that device
- * current); make that first call before any stream capture.  Each call clears
- * the counters it uses on `stream` before use.  All calls share the one
+ * The call allocates and frees nothing.  On its first call on a device that
+ * uses the array it looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * Small batches (at most 128 tokens whose T*k <= 1024 slots form one sort
+ * block, routed by one CTA) do not use the array.  Each call clears the
+ * counters it uses on `stream` before use.  All calls share the one
  * array: calls whose work overlaps on the GPU (different streams without
  * ordering between them) race on it and give wrong results.
  */
