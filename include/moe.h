@@ -158,8 +158,9 @@ moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
  * The call allocates and frees nothing.  On its first call on a device that
  * uses the array it looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.
- * Small batches (at most 128 tokens whose T*k <= 1024 slots form one sort
- * block, routed by one CTA) do not use the array.  Each call clears the
+ * Small batches, which one CTA routes and sorts, do not use the array: those
+ * with T*k <= 1024 and ceil(T/32) * v <= 4, v = 1, 2, 4 or 8 for E up to 32,
+ * 64, 128 or 256.  Each call clears the
  * counters it uses on `stream` before use.  All calls share the one
  * array: calls whose work overlaps on the GPU (different streams without
  * ordering between them) race on it and give wrong results.
