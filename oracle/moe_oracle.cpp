@@ -24,9 +24,13 @@
 // e4m3) because that arithmetic decides the bytes.
 //
 // Parity pins (all in the CPU test-suite): e4m3 codec against torch's
-// float8_e4m3fn and the format definition; top-k and the stable sort against
-// brute force; quantisation against exact special cases; the layer against
-// a float64 per-token expert loop and a dense SwiGLU MLP (E = 1, k = 1).
+// float8_e4m3fn and the format definition; bf16 rounding against torch's
+// float32 -> bfloat16 conversion on every upper half and hand-worked ties;
+// top-k and the stable sort against brute force; quantisation against exact
+// special cases; the permute of e4m3 rows and their scale rows against numpy
+// indexing by token; the bf16 layer against a float64 per-token expert loop
+// and a dense SwiGLU MLP (E = 1, k = 1); the FP8 layer against a float64
+// per-token loop with torch's codecs.
 
 #include <algorithm>
 #include <cmath>

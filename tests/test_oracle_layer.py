@@ -142,3 +142,118 @@ def test_fp8_layer_close_to_bf16_layer():
     live = np.abs(ref).max(1) > 0
     # two e4m3 roundings (2^-4 relative each) on operands and on h
     assert rel[live].max() < 0.2 and np.median(rel[live]) < 0.1 and np.all(out8[~live] == 0)
+
+
+@pytest.mark.parametrize("k", [1, 3, 8])
+def test_permute_moves_fp8_rows_and_their_scales_by_token(k):
+    # the scale rows follow the byte rows: xs[p] = s[sorted_rows[p] // k], and
+    # rows at or past L (sentinels sort last) are not written
+    wl = synth.Workload("ps", T=45, E=12, k=k, H=384, I=128, n_sentinel=min(9, 45 * k - 1))
+    q, s = oracle.quant_act_fp8(synth.hidden_states(wl))
+    ids, _ = oracle.route_topk(synth.router_logits(wl), None, k)
+    ids = oracle.mark_sentinels(ids, synth.sentinel_mask(wl), wl.E)
+    sr, _, off = oracle.sort_by_expert(ids, wl.E)
+    L = int(off[-1])
+    assert L == wl.R - wl.n_sentinel
+    xp, xs = oracle.permute(q, k, sr, L, x_scales=s)
+    tok = sr[:L] // k
+    assert np.array_equal(xp[:L], q[tok]) and np.array_equal(xs[:L], s[tok])
+    assert not np.any(xp[L:]) and not np.any(xs[L:])
+    # the scale rows are those of the tokens, not of the slots
+    if k > 1:
+        assert not np.array_equal(xs[:L], s[np.minimum(sr[:L], wl.T - 1)])
+
+
+def _torch_e4m3_bits(v):
+    """e4m3 codes of fp32 values through PyTorch's float8_e4m3fn conversion
+    (round to nearest even).  A quotient v / (amax / 448) can exceed 448 by an
+    ulp or so when the scale rounded down; below 464, the midpoint to the next
+    (NaN) code, PyTorch rounds it to 448 like a saturating conversion."""
+    v = np.ascontiguousarray(v, np.float32)
+    assert np.all(np.abs(v) < 464.0)
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_e4m3_values(q):
+    return torch.from_numpy(np.ascontiguousarray(q, np.uint8)).view(torch.float8_e4m3fn).float() \
+        .numpy().astype(np.float64)
+
+
+def _quant_rows(v32):
+    """Per row and 128-column group: s = amax / 448 in fp32 (1 for a zero
+    group), codes of v / s (fp32 division) through PyTorch's e4m3 codec."""
+    M, K = v32.shape
+    g = v32.reshape(M, K // 128, 128)
+    amax = np.abs(g).max(axis=2)
+    s = np.where(amax == 0, np.float32(1.0), amax / np.float32(448.0)).astype(np.float32)
+    return _torch_e4m3_bits((g / s[..., None]).reshape(M, K)), s
+
+
+def _block_scaled_matvec(a_codes, sa, w_codes, sw):
+    """sum_kb (sa[kb] * sw[n // 128, kb]) * (exact e4m3 partial of block kb),
+    blocks in ascending order, float64."""
+    N, K = w_codes.shape
+    a = _torch_e4m3_values(a_codes)
+    w = _torch_e4m3_values(w_codes)
+    out = np.zeros(N)
+    for kb in range(K // 128):
+        part = w[:, kb * 128:(kb + 1) * 128] @ a[kb * 128:(kb + 1) * 128]
+        scale = np.float64(sa[kb]) * sw[np.arange(N) // 128, kb].astype(np.float64)
+        out += scale * part
+    return out
+
+
+def _fp8_eager(x_bits, q1, s1, q2, s2, ids, w, E, round_h=True):
+    """The FP8 layer token by token, written from the method's description:
+    x quantised per token per 128 columns; for every picked expert a
+    block-scaled gate_up product, silu(gate) * up, h rounded to bf16 and
+    quantised the same way, a block-scaled down product, weighted sum over the
+    picks.  Codecs through PyTorch, arithmetic in float64 (stored fp32 where
+    the layer stores a tensor)."""
+    T, k = ids.shape
+    H = x_bits.shape[1]
+    I = q2.shape[2]
+    qx, sx = _quant_rows(bf16_bits_to_f32(x_bits))
+    out = np.zeros((T, H), np.float32)
+    for t in range(T):
+        acc = np.zeros(H)
+        for j in range(k):
+            e = ids[t, j]
+            if e == E:
+                continue
+            y1 = _block_scaled_matvec(qx[t], sx[t], q1[e], s1[e]).astype(np.float32)
+            g, u = y1[:I].astype(np.float64), y1[I:].astype(np.float64)
+            h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+            if round_h:
+                h = torch.from_numpy(h).to(torch.bfloat16).float().numpy()
+            qh, sh = _quant_rows(h[None, :])
+            y2 = _block_scaled_matvec(qh[0], sh[0], q2[e], s2[e]).astype(np.float32)
+            acc += np.float64(w[t, j]) * y2.astype(np.float64)
+        out[t] = acc.astype(np.float32)
+    return out
+
+
+@pytest.mark.parametrize("name_or_shape", ["tiny-8e-top2", (40, 6, 3, 256, 384, 7)])
+def test_fp8_layer_matches_fp8_eager_loop(name_or_shape):
+    if isinstance(name_or_shape, str):
+        wl = synth.WORKLOADS[name_or_shape]
+    else:
+        T, E, k, H, I, ns = name_or_shape
+        wl = synth.Workload("f8", T=T, E=E, k=k, H=H, I=I, n_sentinel=ns, dtype="fp8", bias="normal0.5")
+    x, W1, W2 = (synth.hidden_states(wl), synth.expert_weights(wl, "w1"),
+                 synth.expert_weights(wl, "w2"))
+    q1, s1 = oracle.quant_weight_fp8(W1)
+    q2, s2 = oracle.quant_weight_fp8(W2)
+    r = oracle.moe_forward(x, q1, q2, W1_scales=s1, W2_scales=s2, E=wl.E, k=wl.k,
+                           logits=synth.router_logits(wl), bias=synth.expert_bias(wl),
+                           sentinel_mask=synth.sentinel_mask(wl))
+    ref = _fp8_eager(x, q1, s1, q2, s2, r["ids"], r["w"], wl.E)
+    live = np.abs(ref).max(1) > 0
+    assert np.all(r["out"][~live] == 0.0)
+    rel = np.abs(r["out"] - ref).max(1)[live] / np.abs(ref).max(1)[live]
+    assert rel.max() < 1e-6, rel.max()
+    # the loop tells the rounding of h apart: without it the layer moves by
+    # far more than the tolerance above
+    unrounded = _fp8_eager(x, q1, s1, q2, s2, r["ids"], r["w"], wl.E, round_h=False)
+    drift = np.abs(unrounded - ref).max(1)[live] / np.abs(ref).max(1)[live]
+    assert drift.max() > 1e-4
