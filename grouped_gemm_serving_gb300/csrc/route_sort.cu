@@ -73,7 +73,10 @@ __device__ __forceinline__ int checked_id(int id, int E, int* err) {
 
 // Routes token t on one warp: the k picks (or the given ids), the weights
 // and the sentinel mask, written to ids/w.  Returns, in lane j < k, the
-// checked id of slot j (a bad id is reported and returned as E).
+// checked id of slot j.  A bad id (a given id outside [0, E], or a pick that
+// NaN logits left unfilled) is reported, returned as E and written back to
+// ids as E, so that the sort, the combine and ids agree that the slot is a
+// sentinel.
 template <int NV>   // logits per lane: E <= 32 * NV
 __device__ __forceinline__ int route_token(const float* __restrict__ logits, const float* __restrict__ bias,
                                            const uint8_t* __restrict__ mask, int32_t* ids,
@@ -131,16 +134,14 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, con
         if (lane < k) {
             w[slot0 + lane] = expf(my_v - mx) / part;
             if (mask && mask[slot0 + lane]) my_id = E;
+            my_id = checked_id(my_id, E, err);
             ids[slot0 + lane] = my_id;
         }
     } else if (lane < k) {
-        my_id = ids[slot0 + lane];
-        if (mask && mask[slot0 + lane]) {
-            my_id = E;
-            ids[slot0 + lane] = E;
-        }
+        const int given = ids[slot0 + lane];
+        my_id = mask && mask[slot0 + lane] ? E : checked_id(given, E, err);
+        if (my_id != given) ids[slot0 + lane] = my_id;
     }
-    if (lane < k) my_id = checked_id(my_id, E, err);
     return my_id;
 }
 
@@ -501,18 +502,20 @@ extern "C" moe_status_t moe_route_sort_noalloc(const float* logits, const float*
                   moe::aligned16(row_pos) && moe::aligned16(offsets));
     MOE_CHECK_ARG(!logits || (moe::aligned16(logits) && moe::aligned16(topk_w)));
     MOE_CHECK_ARG(!expert_bias || moe::aligned16(expert_bias));
-    const SortGeometry g = geometry(T, k);
-    const size_t ints = static_cast<size_t>(g.blocks) * (E + 1);
-    if (ints > kStaticScratchInts) return MOE_ERR_WORKSPACE;   // beyond the static scratch
-    int* err = moe::device_error_word();
-    if (!err) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (use_small(T, E, k)) {
+    if (use_small(T, E, k)) {   // one CTA, shared memory only: the static array is not used
+        int* err = moe::device_error_word();
+        if (!err) return MOE_ERR_CUDA;
         launch_small(s, logits, logits ? expert_bias : nullptr, sentinel_mask, topk_ids, topk_w, T, E, k,
                      renormalize, sorted_rows, row_pos, offsets, err);
         MOE_CHECK_LAUNCH();
         return MOE_OK;
     }
+    const SortGeometry g = geometry(T, k);
+    const size_t ints = static_cast<size_t>(g.blocks) * (E + 1);
+    if (ints > kStaticScratchInts) return MOE_ERR_WORKSPACE;   // beyond the static scratch
+    int* err = moe::device_error_word();
+    if (!err) return MOE_ERR_CUDA;
     int* counts = static_scratch();
     if (!counts) return MOE_ERR_CUDA;
 

@@ -30,6 +30,10 @@
  *     stream); the functions do not synchronise, allocate or free device
  *     memory, except moe_get_device_error (which synchronises the stream) and
  *     moe_forward with MOE_FWD_HOST_IO (which enqueues host<->device copies).
+ *   - Devices: the library looks up, once per device, the device addresses
+ *     of its own device variables (the error word below, and the static
+ *     array of moe_route_sort_noalloc) and keeps them for the life of the
+ *     process; a cudaDeviceReset of a device makes them stale.
  *   - Errors: host-side argument checks run before any launch and return
  *     MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE with
  *     nothing enqueued; a failed launch returns MOE_ERR_CUDA.  Conditions
@@ -119,9 +123,13 @@ moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream);
  *              pick (renormalize == 0).  topk_ids/topk_w are then outputs.
  *              -0 and +0 tie.  A NaN l' is never picked: a token with fewer
  *              than k other values gets an invalid pick, which is recorded as
- *              MOE_DEVERR_ROUTE and sorted as a sentinel.
+ *              MOE_DEVERR_ROUTE, written to topk_ids as E and sorted as a
+ *              sentinel.
  *              When NULL, topk_ids is an input (ids in [0, E]; E = sentinel)
- *              and topk_w is not touched (may be NULL).
+ *              and topk_w is not touched (may be NULL).  An input id outside
+ *              [0, E] is recorded as MOE_DEVERR_ROUTE and overwritten with E
+ *              (so the sort, moe_combine and topk_ids agree that the slot is
+ *              a sentinel).
  * expert_bias  fp32 [E] or NULL.
  * sentinel_mask uint8 [T*k] or NULL: slots with a nonzero byte get id E.
  * topk_ids     int32 [T, k].   topk_w  fp32 [T, k].
@@ -158,12 +166,15 @@ moe_status_t moe_route_sort(const float* logits, const float* expert_bias,
  * The call allocates and frees nothing.  On its first call on a device that
  * uses the array it looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.
- * Small batches, which one CTA routes and sorts, do not use the array: those
- * with T*k <= 1024 and ceil(T/32) * v <= 4, v = 1, 2, 4 or 8 for E up to 32,
- * 64, 128 or 256.  Each call clears the
- * counters it uses on `stream` before use.  All calls share the one
- * array: calls whose work overlaps on the GPU (different streams without
- * ordering between them) race on it and give wrong results.
+ * The address is kept for the life of the process: a cudaDeviceReset of that
+ * device makes it stale, so do not reset a device this library has run on.
+ * Small batches, which one CTA routes and sorts in shared memory, do not use
+ * the array (nor the size limit above): those with T*k <= 1024 and
+ * ceil(T/32) * v <= 4, where v = 1, 2 or 4 for E up to 32, 64 or 128.  A
+ * batch with E > 128 always uses the array.  Each call clears the counters it
+ * uses on `stream` before use.  All calls share the one array: calls whose
+ * work overlaps on the GPU (different streams without ordering between them)
+ * race on it and give wrong results.
  */
 moe_status_t moe_route_sort_noalloc(const float* logits, const float* expert_bias,
                                     const uint8_t* sentinel_mask, int32_t* topk_ids,

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from grouped_gemm_serving_gb300 import build as gbuild
 
@@ -16,6 +17,15 @@ def moe():
     gbuild.build()
     from grouped_gemm_serving_gb300 import moe as m
     return m
+
+
+# The rejection tests below pass small integers as device pointers: they
+# check that the host-side checks refuse the call before anything is
+# launched.  They run only where no kernel can launch (no GPU), so that a
+# regression in the order of those checks fails an assertion instead of
+# launching a kernel on a bogus address.
+host_only = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake-pointer rejection tests run only without a GPU")
 
 
 def _declared():
@@ -58,6 +68,7 @@ def test_workspace_sizes(moe):
     assert moe.moe_forward_workspace_size(bad) == 0   # FP8 needs multiples of 128 and scales
 
 
+@host_only
 @pytest.mark.parametrize("call", [
     # (function, args) that must fail host-side with MOE_ERR_INVALID_ARG
     ("moe_route_sort", (None, None, None, None, None, 0, 8, 2, 1, None, None, None, None, 0, None)),
@@ -91,11 +102,13 @@ def test_host_side_argument_checks(moe, call):
     assert getattr(moe.lib(), name)(*args) == moe.MOE_ERR_INVALID_ARG
 
 
+@host_only
 def test_bf16_quantising_epilogue_is_unsupported(moe):
     st = moe.lib().moe_grouped_gemm(0, 16, None, 16, None, 16, 8, 64, 256, 64, 2, 16, None, None)
     assert st == moe.MOE_ERR_UNSUPPORTED
 
 
+@host_only
 def test_gather_needs_whole_128_byte_k_blocks(moe):
     # bf16 K = 200 is 400 bytes per row: not a whole number of k-blocks
     st = moe.lib().moe_grouped_gemm_gather(0, 16, None, 4, 2, 16, 16, None, 16, 8, 64, 64, 200, 0, 16, None, None)
@@ -114,11 +127,24 @@ def test_forward_gathers_only_whole_k_blocks(moe):
     assert sep == gat + 64 * 2 * 256 * 2
 
 
+@host_only
 def test_workspace_too_small_is_reported(moe):
     st = moe.lib().moe_route_sort(16, None, None, 16, 16, 64, 8, 2, 1, 16, 16, 16, 16, 4, None)
     assert st == moe.MOE_ERR_WORKSPACE
 
 
+@host_only
 def test_selftest_limit_is_checked_on_host(moe):
     assert moe.lib().moe_selftest_wait_timeout(0, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.lib().moe_selftest_wait_timeout(3_000_000_000, None) == moe.MOE_ERR_INVALID_ARG
+
+
+@host_only
+def test_noalloc_rejects_requests_beyond_its_scratch(moe):
+    # E = 256, k = 8: 128 tokens per sort block, 257 counters each; 256 KiB of
+    # counters hold 255 blocks, so 32768 tokens (256 blocks) are refused
+    lib = moe.lib()
+    st = lib.moe_route_sort_noalloc(16, None, None, 16, 16, 32768, 256, 8, 1, 16, 16, 16, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    st = lib.moe_route_sort_noalloc(16, None, None, 16, 16, 600000, 256, 8, 1, 16, 16, 16, None)
+    assert st == moe.MOE_ERR_WORKSPACE

@@ -126,6 +126,8 @@ def test_bad_expert_id_is_reported_not_placed(moe):
     sr = host(r["sorted_rows"])
     assert np.array_equal(np.sort(sr), np.arange(128))       # still a permutation
     assert host(r["offsets"])[-1] == 127                     # the bad slot sorts as a sentinel
+    got = host(r["ids"])                                     # and reads as one in topk_ids
+    assert got[5, 0] == 8 and np.array_equal(np.delete(got.reshape(-1), 10), np.delete(ids.reshape(-1), 10))
 
 
 def test_route_never_picks_nan(moe):
@@ -155,6 +157,7 @@ def test_route_too_few_numbers_is_reported(moe):
     assert np.array_equal(np.sort(host(r["sorted_rows"])), np.arange(T * k))
     assert host(r["offsets"])[-1] == T * k - 2
     assert set(host(r["ids"])[7, :2]) == {0, 1}
+    assert np.all(host(r["ids"])[7, 2:] == E)               # unfilled picks read as sentinels
 
 
 # ---------------------------------------------------------------- FP8 quantisation
