@@ -1,10 +1,15 @@
 """Full-size parity: every layer workload at its real size, run through
 moe_forward exactly as bench.py launches it, checked against the oracle
 on all routing outputs (bit-exact) and on sampled tokens (the oracle computes
-those tokens one by one; a token's output depends only on its own row).
+those tokens one by one; a token's output depends only on its own row).  The
+sample reaches every expert: each expert's first and last routed token (the
+last one in the expert's last, partial tile), plus random tokens.
 Also the live-row sweep of the grouped GEMMs (16384 permuted rows, 128
 experts, 100 % / 50 % / 12.5 % live): sampled rows against the oracle and every
 sentinel row exactly zero although its input is NaN."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -16,9 +21,70 @@ from tests.gpu_helpers import (dev, dev_bf16, host, host_bf16_bits, host_f32_fro
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-SAMPLE = {"32e-top4-h2880": 16, "128e-top8-h2048-zipf": 16, "256e-top8-h7168-fp8": 4,
+# random tokens per workload, on top of the first and the last routed token
+# of every expert (the latter lands in the expert's last, partial tile)
+SAMPLE = {"32e-top4-h2880": 16, "128e-top8-h2048-zipf": 16, "256e-top8-h7168-fp8": 8,
           # decode-sized batches of the same layers (64 tokens)
-          "32e-top4-h2880-t64": 16, "256e-top8-h7168-fp8-t64": 4}
+          "32e-top4-h2880-t64": 16, "256e-top8-h7168-fp8-t64": 8}
+CHUNK = 8                                    # experts per oracle call
+THREADS = max(1, min(8, os.cpu_count() or 1))
+
+
+def _sample_tokens(ids, E, k, n_random, seed):
+    """Tokens that reach every expert with rows: each expert's first and last
+    row in expert order (the last row sits in the expert's last tile, the
+    partial one), plus n_random tokens drawn at random."""
+    sr, _, off = oracle.sort_by_expert(ids, E)
+    toks = set(np.random.default_rng(seed).choice(ids.shape[0], n_random, replace=False).tolist())
+    for e in range(E):
+        if off[e + 1] > off[e]:
+            toks.add(int(sr[off[e]]) // k)
+            toks.add(int(sr[off[e + 1] - 1]) // k)
+    S = np.array(sorted(toks))
+    assert set(np.unique(ids[S])) == set(np.nonzero(np.diff(off) > 0)[0].tolist())
+    return S
+
+
+def _oracle_rows(moe, wl, x, ids, w, S, W1_dev, W2_dev, S1_dev, S2_dev):
+    """The oracle's layer output for tokens S, summed over chunks of CHUNK
+    experts (each call sees only its chunk's experts; the other picks are
+    sentinels to it -- the partial-output sum of expert parallelism), chunks in
+    parallel threads.  For FP8 each chunk's weights are quantised by the
+    oracle from the bf16 draws and must equal the library's, bit for bit."""
+    fp8 = wl.dtype == "fp8"
+    used = np.unique(ids[S])
+    chunks = [used[i:i + CHUNK] for i in range(0, used.size, CHUNK)]
+    xs, ids_s, w_s = x[S], ids[S], w[S]
+
+    def run(c):
+        remap = np.full(wl.E + 1, c.size, np.int64)          # other experts: sentinel of the chunk
+        remap[c] = np.arange(c.size)
+        W1h = synth.expert_weights(wl, "w1", experts=c, threads=2)
+        W2h = synth.expert_weights(wl, "w2", experts=c, threads=2)
+        kw = dict(E=int(c.size), k=wl.k, ids=remap[ids_s].astype(np.int32), w=w_s)
+        if not fp8:
+            return oracle.moe_forward(xs, W1h, W2h, **kw)["out"], True
+        q1, s1 = oracle.quant_weight_fp8(W1h)
+        q2, s2 = oracle.quant_weight_fp8(W2h)
+        del W1h, W2h
+        same = all(np.array_equal(host(dv[c]), hv) for dv, hv in
+                   ((W1_dev, q1), (W2_dev, q2), (S1_dev, s1), (S2_dev, s2)))
+        return oracle.moe_forward(xs, q1, q2, W1_scales=s1, W2_scales=s2, **kw)["out"], same
+
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(run, chunks))
+    assert all(same for _, same in parts), "library FP8 weight quantiser differs from the oracle's"
+    return np.sum([p.astype(np.float64) for p, _ in parts], axis=0)
+
+
+def _group_rel_err(y, ref, group=128):
+    """Per row and 128-column group (the last one may be short):
+    max |y - ref| / max |ref| over the group."""
+    n = ref.shape[1]
+    errs = []
+    for c0 in range(0, n, group):
+        errs.append(row_rel_err(y[:, c0:c0 + group], ref[:, c0:c0 + group]))
+    return np.stack(errs, axis=1)
 
 
 @pytest.fixture(scope="module")
@@ -70,29 +136,17 @@ def test_full_size_layer(moe, name):
     assert np.array_equal(host(ids_d), ids)
     np.testing.assert_allclose(host(w_d), w, rtol=2e-6)
 
-    # sampled tokens through the oracle, with only the experts they use
-    g = np.random.default_rng(123)
-    S = np.sort(g.choice(wl.T, SAMPLE[name], replace=False))
-    used = np.unique(ids[S])
-    remap = np.full(wl.E + 1, -1, np.int64)
-    remap[used] = np.arange(used.size)
-    ids_c = remap[ids[S]].astype(np.int32)
-    W1h = synth.expert_weights(wl, "w1", experts=used)
-    W2h = synth.expert_weights(wl, "w2", experts=used)
-    kw = dict(E=int(used.size), k=wl.k, ids=ids_c, w=w[S])
-    if fp8:
-        q1, s1 = oracle.quant_weight_fp8(W1h)
-        q2, s2 = oracle.quant_weight_fp8(W2h)
-        e0 = int(used[0])                                    # the library's weight quantiser agrees
-        assert np.array_equal(host(W1[e0]), q1[0]) and np.array_equal(host(S2[e0]), s2[0])
-        ref = oracle.moe_forward(x[S], q1, q2, W1_scales=s1, W2_scales=s2, **kw)["out"]
-        tol = 4e-2
-    else:
-        ref = oracle.moe_forward(x[S], W1h, W2h, **kw)["out"]
-        tol = 2e-2
+    # sampled tokens through the oracle: every expert's first and last row
+    S = _sample_tokens(ids, wl.E, wl.k, SAMPLE[name], seed=123)
+    ref = _oracle_rows(moe, wl, x, ids, w, S, W1, W2, S1, S2)
+    tol = 4e-2 if fp8 else 2e-2
     got = host_f32_from_bf16(out)[S]
     err = row_rel_err(got, ref)
     assert err.max() <= tol, (name, err.max())
+    # and every 128-column group on its own, the short tail group included
+    # (H = 2880 = 22 * 128 + 64), against the group's own largest value
+    gerr = _group_rel_err(got, ref)
+    assert gerr.max() <= 2 * tol, (name, np.unravel_index(gerr.argmax(), gerr.shape), gerr.max())
 
 
 @pytest.mark.parametrize("live", [16384, 8192, 2048])
