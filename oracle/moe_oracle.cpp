@@ -23,6 +23,12 @@
 // quantisation is done in fp32 (amax, two IEEE divides, one rounding to
 // e4m3) because that arithmetic decides the bytes.
 //
+// Threads: the loops over independent rows carry OpenMP pragmas.  The
+// default build (no -fopenmp) ignores them and runs on one core; the timing
+// build of the CPU baseline adds -fopenmp and runs the rows in parallel.  Each
+// output element is computed by one thread in the same order either way, so
+// the two builds agree bit for bit (a CPU test checks that).
+//
 // Parity pins (all in the CPU test-suite): e4m3 codec against torch's
 // float8_e4m3fn and the format definition; bf16 rounding against torch's
 // float32 -> bfloat16 conversion on every upper half and hand-worked ties;
@@ -34,6 +40,9 @@
 
 #include <algorithm>
 #include <cmath>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <cstdint>
 #include <cstring>
 #include <vector>
@@ -111,6 +120,15 @@ inline float fp8_scale_from_amax(float amax) {
 
 extern "C" {
 
+// Threads the row loops run on: 1 in the default build.
+int orc_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
 // ---------------------------------------------------------------- e4m3 codec
 void orc_e4m3_encode(const float* v, int64_t n, uint8_t* q) {
     for (int64_t i = 0; i < n; ++i) q[i] = e4m3_encode(v[i]);
@@ -133,9 +151,10 @@ void orc_bf16_round(const float* v, int64_t n, uint16_t* out) {
 // E evaluated at the picks (renormalize == 0), in double, stored fp32.
 void orc_route_topk(const float* logits, const float* bias, int T, int E, int k,
                     int renormalize, int32_t* ids, float* w) {
-    std::vector<float> lp(E);
-    std::vector<char> taken(E);
+#pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t) {
+        std::vector<float> lp(E);
+        std::vector<char> taken(E);
         for (int e = 0; e < E; ++e)
             lp[e] = bias ? logits[(int64_t)t * E + e] + bias[e] : logits[(int64_t)t * E + e];
         std::fill(taken.begin(), taken.end(), 0);
@@ -198,6 +217,7 @@ void orc_sort_by_expert(const int32_t* ids, int64_t R, int E, int32_t* sorted_ro
 // x is bf16 [M, K], K a multiple of 128; q is [M, K]; s is fp32 [M, K/128].
 void orc_quant_act_fp8(const uint16_t* x, int64_t M, int K, uint8_t* q, float* s) {
     const int G = K / 128;
+#pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; ++m) {
         for (int g = 0; g < G; ++g) {
             const uint16_t* xr = x + m * K + g * 128;
@@ -216,11 +236,12 @@ void orc_quant_act_fp8(const uint16_t* x, int64_t M, int K, uint8_t* q, float* s
 // s is [E, ceil(N/128), K/128].
 void orc_quant_weight_fp8(const uint16_t* W, int E, int N, int K, uint8_t* q, float* s) {
     const int NB = (N + 127) / 128, KB = K / 128;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int e = 0; e < E; ++e) {
-        const uint16_t* We = W + (int64_t)e * N * K;
-        uint8_t* qe = q + (int64_t)e * N * K;
         for (int nb = 0; nb < NB; ++nb) {
-            int n1 = std::min(N, nb * 128 + 128);
+            const uint16_t* We = W + (int64_t)e * N * K;
+            uint8_t* qe = q + (int64_t)e * N * K;
+            const int n1 = std::min(N, nb * 128 + 128);
             for (int kb = 0; kb < KB; ++kb) {
                 float amax = 0.0f;
                 for (int n = nb * 128; n < n1; ++n)
@@ -244,6 +265,7 @@ void orc_quant_weight_fp8(const uint16_t* W, int E, int N, int K, uint8_t* q, fl
 void orc_permute(const void* x, const float* x_scales, int elem_bytes, int64_t T, int H, int k,
                  const int32_t* sorted_rows, int64_t L, void* xp, float* xp_scales) {
     const int G = H / 128;
+#pragma omp parallel for schedule(static)
     for (int64_t p = 0; p < L; ++p) {
         int64_t t = sorted_rows[p] / k;
         std::memcpy(static_cast<char*>(xp) + p * H * elem_bytes,
@@ -271,7 +293,7 @@ void orc_grouped_gemm_bf16(const uint16_t* A, const uint16_t* B, const int32_t* 
                            int64_t M_cap, int N, int K, const int32_t* rows, int64_t n_rows,
                            float* C) {
     int64_t nout = rows ? n_rows : M_cap;
-    std::vector<float> a(K);
+#pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < nout; ++i) {
         int64_t p = rows ? rows[i] : i;
         float* Ci = C + i * N;
@@ -280,6 +302,7 @@ void orc_grouped_gemm_bf16(const uint16_t* A, const uint16_t* B, const int32_t* 
             for (int n = 0; n < N; ++n) Ci[n] = 0.0f;
             continue;
         }
+        std::vector<float> a(K);
         for (int c = 0; c < K; ++c) a[c] = bf16_to_f32(A[p * K + c]);
         const uint16_t* Be = B + (int64_t)e * N * K;
         for (int n = 0; n < N; ++n) {
@@ -300,8 +323,8 @@ void orc_grouped_gemm_bf16(const uint16_t* A, const uint16_t* B, const int32_t* 
 void orc_grouped_gemm_dgrad_bf16(const uint16_t* dC, const uint16_t* B, const int32_t* offsets, int E,
                                  int64_t M_cap, int N, int K, const int32_t* rows, int64_t n_rows,
                                  float* dA) {
-    std::vector<double> acc(K);
     const int64_t nout = rows ? n_rows : M_cap;
+#pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < nout; ++i) {
         const int64_t p = rows ? rows[i] : i;
         float* dAp = dA + i * K;
@@ -310,7 +333,7 @@ void orc_grouped_gemm_dgrad_bf16(const uint16_t* dC, const uint16_t* B, const in
             for (int c = 0; c < K; ++c) dAp[c] = 0.0f;
             continue;
         }
-        std::fill(acc.begin(), acc.end(), 0.0);
+        std::vector<double> acc(K, 0.0);
         const uint16_t* Be = B + (int64_t)e * N * K;
         for (int n = 0; n < N; ++n) {
             const double g = bf16_to_f32(dC[p * N + n]);
@@ -328,12 +351,12 @@ void orc_grouped_gemm_wgrad_bf16(const uint16_t* A, const uint16_t* dC, const in
                                  int64_t M_cap, int N, int K, const int32_t* pairs, int64_t n_pairs,
                                  float* dB) {
     (void)M_cap;
-    std::vector<double> acc(K);
     const int64_t nout = pairs ? n_pairs : (int64_t)E * N;
+#pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < nout; ++i) {
         const int e = pairs ? pairs[2 * i] : (int)(i / N);
         const int n = pairs ? pairs[2 * i + 1] : (int)(i % N);
-        std::fill(acc.begin(), acc.end(), 0.0);
+        std::vector<double> acc(K, 0.0);
         for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
             const double g = bf16_to_f32(dC[p * N + n]);
             for (int c = 0; c < K; ++c) acc[c] += g * (double)bf16_to_f32(A[p * K + c]);
@@ -351,7 +374,8 @@ void orc_grouped_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb,
                           const int32_t* rows, int64_t n_rows, float* C) {
     const int KB = K / 128, NB = (N + 127) / 128;
     int64_t nout = rows ? n_rows : M_cap;
-    std::vector<float> a(K);
+    const float* dec = e4m3_table();
+#pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < nout; ++i) {
         int64_t p = rows ? rows[i] : i;
         float* Ci = C + i * N;
@@ -360,7 +384,7 @@ void orc_grouped_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb,
             for (int n = 0; n < N; ++n) Ci[n] = 0.0f;
             continue;
         }
-        const float* dec = e4m3_table();
+        std::vector<float> a(K);
         for (int c = 0; c < K; ++c) a[c] = dec[qa[p * K + c]];
         const uint8_t* Be = qb + (int64_t)e * N * K;
         for (int n = 0; n < N; ++n) {
@@ -381,6 +405,7 @@ void orc_grouped_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb,
 // gate = Y1[p, :I] (first half of W1's rows), up = Y1[p, I:].  Rows at or
 // beyond L are zero.
 void orc_swiglu(const float* Y1, int64_t M_cap, int I, int64_t L, float* h) {
+#pragma omp parallel for schedule(static)
     for (int64_t p = 0; p < M_cap; ++p) {
         for (int n = 0; n < I; ++n) {
             if (p >= L) { h[p * I + n] = 0.0f; continue; }
@@ -397,9 +422,9 @@ void orc_swiglu(const float* Y1, int64_t M_cap, int I, int64_t L, float* h) {
 // in j order.  A token whose slots are all sentinels gets a zero row.
 void orc_combine(const float* Y2, const int32_t* ids, const float* w, const int32_t* row_pos,
                  int64_t T, int k, int H, int E, float* out) {
-    std::vector<double> acc(H);
+#pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
-        std::fill(acc.begin(), acc.end(), 0.0);
+        std::vector<double> acc(H, 0.0);
         for (int j = 0; j < k; ++j) {
             int64_t f = t * k + j;
             if (ids[f] == E) continue;
@@ -438,6 +463,7 @@ int orc_moe_forward(int fp8, const float* logits, const float* bias, const uint8
                               2 * I, H, nullptr, 0, Y1.data());
         orc_swiglu(Y1.data(), R, I, L, h.data());
         // the plain definition keeps h in fp32; the down GEMM reads it directly
+#pragma omp parallel for schedule(dynamic, 4)
         for (int64_t p = 0; p < R; ++p) {
             int e = expert_of_row(offsets.data(), E, p);
             float* y = Y2.data() + p * H;

@@ -14,34 +14,52 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.cpp")
-_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+_LIBS = {False: os.path.join(_HERE, "libmoe_oracle.so"),       # one core
+         True: os.path.join(_HERE, "libmoe_oracle_omp.so")}    # OpenMP over rows
 
 __all__ = [
-    "build", "e4m3_encode", "e4m3_decode", "bf16_round", "route_topk", "mark_sentinels",
-    "sort_by_expert", "quant_act_fp8", "quant_weight_fp8", "permute", "grouped_gemm_bf16",
-    "grouped_gemm_fp8", "swiglu", "combine", "moe_forward", "grouped_gemm_dgrad_bf16",
-    "grouped_gemm_wgrad_bf16",
+    "build", "use_openmp", "threads", "e4m3_encode", "e4m3_decode", "bf16_round", "route_topk",
+    "mark_sentinels", "sort_by_expert", "quant_act_fp8", "quant_weight_fp8", "permute",
+    "grouped_gemm_bf16", "grouped_gemm_fp8", "swiglu", "combine", "moe_forward",
+    "grouped_gemm_dgrad_bf16", "grouped_gemm_wgrad_bf16",
 ]
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with g++ (no fast-math, no FMA contraction)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile the oracle with g++ (no fast-math, no FMA contraction).  With
+    openmp, the same source with -fopenmp: its row loops run on all cores,
+    each output element still computed by one thread in the same order."""
+    lib = _LIBS[bool(openmp)]
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_SRC):
         cmd = ["g++", "-O2", "-std=c++17", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
-               "-shared", _SRC, "-o", _LIB + ".tmp"]
+               "-shared"] + (["-fopenmp"] if openmp else []) + [_SRC, "-o", lib + ".tmp"]
         subprocess.check_call(cmd)
-        os.replace(_LIB + ".tmp", _LIB)
-    return _LIB
+        os.replace(lib + ".tmp", lib)
+    return lib
 
 
-_lib = None
+_lib = {}
+_openmp = False
+
+
+def use_openmp(on: bool = True) -> bool:
+    """Route every function of this module to the OpenMP build (on) or the
+    one-core build (off); returns the previous setting."""
+    global _openmp
+    prev, _openmp = _openmp, bool(on)
+    return prev
 
 
 def _L():
-    global _lib
-    if _lib is None:
-        _lib = C.CDLL(build())
-    return _lib
+    lib = _lib.get(_openmp)
+    if lib is None:
+        lib = _lib[_openmp] = C.CDLL(build(openmp=_openmp))
+    return lib
+
+
+def threads() -> int:
+    """Threads the active build runs its row loops on (1 for the one-core build)."""
+    return int(_L().orc_threads())
 
 
 def _p(a):
