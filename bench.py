@@ -39,8 +39,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-sample-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure the headline workload only (skip the other workloads' record)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels one by one instead of replaying a CUDA graph")
     ap.add_argument("--grad", action="store_true",
@@ -165,6 +166,8 @@ def make_layer(wl, torch, moe, synth):
     L["x"] = bf16_dev(L["x_host"])
     L["logits"] = torch.from_numpy(L["logits_host"]).to(dev)
     L["bias"] = None if bias is None else torch.from_numpy(bias).to(dev)
+    mask = synth.sentinel_mask(wl)
+    L["mask"] = None if mask is None else torch.from_numpy(mask).to(dev)
     fp8 = wl.dtype == "fp8"
     for which, (n, kdim) in (("w1", (2 * wl.I, wl.H)), ("w2", (wl.H, wl.I))):
         if not fp8:
@@ -226,7 +229,7 @@ class Step:
         ev = iter(self.ev)
         mark = (lambda: next(ev).record()) if record else (lambda: None)
         mark()
-        moe.moe_route_sort(L["logits"], L["bias"], None, self.ids, self.w, T, E, k, wl.renormalize,
+        moe.moe_route_sort(L["logits"], L["bias"], L["mask"], self.ids, self.w, T, E, k, wl.renormalize,
                            self.sr, self.rp, self.off, self.rws, self.rws_bytes)
         mark()
         if self.fp8:
@@ -269,32 +272,141 @@ class Step:
 
 def flops_bytes(wl, live_rows, experts_live, separate_scatter=False):
     """Algorithmic work of one step: GEMM FLOPs on live rows and the minimum
-    HBM bytes of each kernel (weights of experts with rows, activations once).
-    The gathered gate_up GEMM reads x itself: each token row once at least."""
+    HBM bytes of each kernel (weights of experts with rows, with their block
+    scales for FP8; activations once).  The gathered gate_up GEMM reads x
+    itself: each token row once at least."""
     T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
     R = T * k
-    wb = 1 if wl.dtype == "fp8" else 2
-    ab = 1 if wl.dtype == "fp8" else 2
+    fp8 = wl.dtype == "fp8"
+    wb = 1 if fp8 else 2
+    ab = 1 if fp8 else 2
+    w1 = 2 * I * H * wb + (2 * I // 128) * (H // 128) * 4 * fp8
+    w2 = H * I * wb + -(-H // 128) * (I // 128) * 4 * fp8
+    sa = (H // 128) * 4 * fp8          # activation scales per row of x (FP8)
+    sh = (I // 128) * 4 * fp8          # ... of h
     f1 = 2.0 * live_rows * (2 * I) * H
     f2 = 2.0 * live_rows * H * I
-    b1 = experts_live * 2 * I * H * wb + (live_rows if separate_scatter else T) * H * ab + live_rows * I * ab
-    b2 = experts_live * H * I * wb + live_rows * I * ab + R * H * 2
-    bp = T * H * ab + live_rows * H * ab
+    b1 = (experts_live * w1 + (live_rows if separate_scatter else T) * (H * ab + sa)
+          + live_rows * (I * ab + sh) + (R - live_rows) * (I * ab + sh))
+    b2 = experts_live * w2 + live_rows * (I * ab + sh) + R * H * 2
+    bp = T * (H * ab + sa) + live_rows * (H * ab + sa)
     bc = live_rows * H * 2 + R * 12 + T * H * 2
+    bq = T * H * 2 + T * H + T * (H // 128) * 4
+    br = T * E * 4 + R * 20
     return dict(gemm1_flop=f1, gemm2_flop=f2, gemm1_bytes=b1, gemm2_bytes=b2, permute_bytes=bp,
-                combine_bytes=bc)
+                combine_bytes=bc, act_quant_bytes=bq, route_bytes=br)
+
+
+def layer_summary(wl, step, step_ms, separate, pk):
+    """Per-layer figures from the timed steps: step time and tokens/s, and per
+    kernel its time with its fraction of the bound that applies -- the tensor
+    peak (bf16, or 2 x bf16 for FP8) and the HBM copy bandwidth for the grouped
+    GEMMs (and the larger of the two as the roofline), HBM for the data-movement
+    kernels."""
+    off = step.off.cpu().numpy()
+    live = int(off[-1])
+    experts_live = int((np.diff(off) > 0).sum())
+    fb = flops_bytes(wl, live, experts_live, separate)
+    kt = {n: statistics.fmean(v) for n, v in step.times.items()}
+    fp8 = wl.dtype == "fp8"
+    tpeak = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    hbm = pk["hbm_gbs"]
+    gemm = {}
+    for name, key, fl, by in (("gate_up", "gemm_gate_up_swiglu", fb["gemm1_flop"], fb["gemm1_bytes"]),
+                              ("down", "gemm_down", fb["gemm2_flop"], fb["gemm2_bytes"])):
+        t = kt[key] * 1e-3
+        gemm[name] = {"ms": kt[key], "tflops": fl / t / 1e12, "tensor_frac": fl / t / 1e12 / tpeak,
+                      "hbm_gbs": by / t / 1e9, "hbm_frac": by / t / 1e9 / hbm,
+                      "roofline_frac": max(fl / (tpeak * 1e12), by / (hbm * 1e9)) / t,
+                      "algorithmic_flop": fl, "algorithmic_bytes": by}
+    data = {}
+    for name, key in (("route_sort", "route_bytes"), ("act_quant", "act_quant_bytes"),
+                      ("permute", "permute_bytes"), ("combine", "combine_bytes")):
+        if name in kt:
+            gbs = fb[key] / (kt[name] * 1e-3) / 1e9
+            data[name] = {"ms": kt[name], "gbs": gbs, "hbm_frac": gbs / hbm, "algorithmic_bytes": fb[key]}
+    ms = statistics.fmean(step_ms)
+    return {"ms_per_step": ms, "tokens_per_s": wl.T / (ms * 1e-3), "live_rows": live,
+            "experts_with_rows": experts_live, "kernels_ms": kt, "gemm": gemm, "data_movement": data,
+            "peaks": {"tensor_tflops": tpeak, "hbm_gbs": hbm,
+                      "tensor_source": ("fp8 = 2 x " if fp8 else "") + "measured bf16 burst (cuBLAS)"},
+            "_fb": fb}
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_tokens_per_s(wl, sample_tokens, x_host, logits_host, bias_host, W1, W2, W1s=None, W2s=None):
+# multiply-adds of the oracle's budget for one timed sample: all-core and one core
+CPU_MACS_ALL = 40e9
+CPU_MACS_ONE = 3e9
+
+
+def oracle_weights(wl, synth, used, chunk=16):
+    """Host weights for the oracle: full [E, ...] stacks of which only the
+    experts in `used` are drawn (the others are never written, and never read:
+    the oracle runs only the experts its tokens pick).  FP8 weights are
+    quantised by the oracle, chunk by chunk."""
     import oracle
-    xs = x_host[:sample_tokens]
-    ls = logits_host[:sample_tokens]
-    t0 = time.perf_counter()
-    oracle.moe_forward(xs, W1, W2, E=wl.E, k=wl.k, logits=ls, bias=bias_host,
-                       renormalize=wl.renormalize, W1_scales=W1s, W2_scales=W2s)
-    dt = time.perf_counter() - t0
-    return sample_tokens / dt, dt
+    fp8 = wl.dtype == "fp8"
+    out = []
+    for which, (n, kdim) in (("w1", (2 * wl.I, wl.H)), ("w2", (wl.H, wl.I))):
+        W = np.empty((wl.E, n, kdim), np.uint8 if fp8 else np.uint16)
+        S = np.empty((wl.E, -(-n // 128), kdim // 128), np.float32) if fp8 else None
+        for i in range(0, len(used), chunk):
+            ex = np.asarray(used[i:i + chunk])
+            bf = synth.expert_weights(wl, which, experts=ex)
+            if fp8:
+                W[ex], S[ex] = oracle.quant_weight_fp8(bf)
+            else:
+                W[ex] = bf
+        out += [W, S]
+    return out[0], out[2], out[1], out[3]
+
+
+def oracle_layer_rate(wl, synth, n_one=None, n_all=None):
+    """The oracle, as it stands, on the first tokens of the workload: one
+    whole layer (route, sort, [quantise], permute, both GEMMs, combine) per
+    call, timed on one core (one-core build) and on every host core (OpenMP
+    build).  Sample sizes follow a fixed multiply-add budget unless given."""
+    import oracle
+    macs = wl.k * 3 * wl.H * wl.I
+    n_all = n_all or int(min(wl.T, max(8, CPU_MACS_ALL // macs)))
+    n_one = n_one or int(min(wl.T, max(2, CPU_MACS_ONE // macs)))
+    if wl.dtype == "fp8":
+        # the experts the sample picks are drawn and quantised first (about 80
+        # of the 256-expert layer's for 12 tokens): that setup dominates
+        n_all, n_one = min(n_all, 12), min(n_one, 4)
+    n = max(n_all, n_one)
+    x, logits, bias = synth.hidden_states(wl)[:n], synth.router_logits(wl)[:n], synth.expert_bias(wl)
+    prev = oracle.use_openmp(True)
+    try:
+        ids, _ = oracle.route_topk(logits, bias, wl.k, wl.renormalize)
+        W1, W2, s1, s2 = oracle_weights(wl, synth, np.unique(ids))
+        res = {}
+        for label, omp, m in (("all", True, n_all), ("one", False, n_one)):
+            oracle.use_openmp(omp)
+            reps, dt = 0, 0.0
+            while dt < 0.5 or reps == 0:          # repeat a tiny sample to at least 0.5 s
+                t0 = time.perf_counter()
+                oracle.moe_forward(x[:m], W1, W2, E=wl.E, k=wl.k, logits=logits[:m], bias=bias,
+                                   renormalize=wl.renormalize, W1_scales=s1, W2_scales=s2)
+                dt += time.perf_counter() - t0
+                reps += 1
+            res[label] = (m * reps / dt, m, reps, dt, oracle.threads())
+    finally:
+        oracle.use_openmp(prev)
+    return res
+
+
+def cpu_baseline_record(wl, synth):
+    cores, model = cpu_info()
+    r = oracle_layer_rate(wl, synth)
+    v, m, reps, dt, thr = r["all"]
+    v1, m1, reps1, dt1, _ = r["one"]
+    return {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "sample": (f"first {m} of {wl.T} tokens of {wl.name}, x{reps} ({dt:.1f} s), "
+                       f"OpenMP build over rows on {thr} threads"),
+            "single_core": {"value": v1, "unit": "tokens/s", "cores": 1,
+                            "sample": f"first {m1} tokens, x{reps1} ({dt1:.1f} s), one-core build"},
+            "cpu": model, "host_cores": cores}
 
 
 def cpu_info():
@@ -314,32 +426,37 @@ def cpu_info():
     return cores, model
 
 
-def host_weights(wl, synth):
-    W1 = synth.expert_weights(wl, "w1")
-    W2 = synth.expert_weights(wl, "w2")
-    if wl.dtype != "fp8":
-        return W1, W2, None, None
-    import oracle
-    q1, s1 = oracle.quant_weight_fp8(W1)
-    q2, s2 = oracle.quant_weight_fp8(W2)
-    return q1, q2, s1, s2
-
-
 def reference_main(args, wl, synth):
-    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    """The reference arm: the CPU oracle, as it stands, on every host core
+    (its OpenMP build), each step one layer over a bounded window of the
+    workload's tokens."""
+    import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    W1, W2, s1, s2 = host_weights(wl, synth)
+    macs = wl.k * 3 * wl.H * wl.I
+    per_step = int(max(1, min(wl.T, 4e9 // macs)))
+    starts = [(i * per_step) % max(1, wl.T - per_step + 1) for i in range(args.warmup + args.steps)]
     x, logits, bias = synth.hidden_states(wl), synth.router_logits(wl), synth.expert_bias(wl)
-    per_step = max(1, min(args.cpu_sample_tokens, 4))
-    for i in range(args.warmup):
-        oracle_tokens_per_s(wl, per_step, x[i * per_step:], logits[i * per_step:], bias, W1, W2, s1, s2)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        j = (i * per_step) % max(1, wl.T - per_step)
-        oracle_tokens_per_s(wl, per_step, x[j:], logits[j:], bias, W1, W2, s1, s2)
-    dt = time.perf_counter() - t0
+    prev = oracle.use_openmp(True)
+    try:
+        ids, _ = oracle.route_topk(np.concatenate([logits[j:j + per_step] for j in starts]), bias, wl.k,
+                                   wl.renormalize)
+        W1, W2, s1, s2 = oracle_weights(wl, synth, np.unique(ids))
+        threads = oracle.threads()
+
+        def one(j):
+            oracle.moe_forward(x[j:j + per_step], W1, W2, E=wl.E, k=wl.k, logits=logits[j:j + per_step],
+                               bias=bias, renormalize=wl.renormalize, W1_scales=s1, W2_scales=s2)
+
+        for j in starts[:args.warmup]:
+            one(j)
+        t0 = time.perf_counter()
+        for j in starts[args.warmup:]:
+            one(j)
+        dt = time.perf_counter() - t0
+    finally:
+        oracle.use_openmp(prev)
     value = per_step * args.steps / dt
     cores, model = cpu_info()
     line = {
@@ -349,8 +466,9 @@ def reference_main(args, wl, synth):
         "data": "synthetic (seeded numpy draws)",
         "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I,
                    "layer_dtype": wl.dtype, "step": f"{per_step} tokens of the workload per step"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} tokens per step x {args.steps} steps of {wl.name}",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": (f"{per_step} tokens per step x {args.steps} steps of {wl.name}, "
+                                    f"OpenMP build over rows on {threads} threads"),
                          "cpu": model, "host_cores": cores},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -359,12 +477,14 @@ def reference_main(args, wl, synth):
 
 
 # ------------------------------------------------------------------ sweep
-def sweep_main(args, synth, torch, moe):
+SWEEP_NAME = "sweep-128e-h2048-i768-m16384"
+
+
+def sweep_measure(steps, warmup, synth, torch, moe, pk):
     """Both grouped GEMMs over 16384 permuted rows of 128 experts (H=2048,
     I=768, bf16) with 100 / 50 / 12.5 % of the rows live: split equally over
     all experts, and concentrated on the first live/128 experts (128 rows
     each).  Sentinel rows are NaN on input; the GEMMs write them as zeros."""
-    pk, pk_kind = peaks()
     base = synth.Sweep()
     wl = base.workload
 
@@ -398,11 +518,11 @@ def sweep_main(args, synth, torch, moe):
                 moe.moe_grouped_gemm(moe.MOE_BF16, h, None, W2, None, off, E, M, H, I, moe.MOE_EPI_STORE, y2,
                                      None)
 
-            for _ in range(max(3, args.warmup)):
+            for _ in range(max(3, warmup)):
                 run()
             torch.cuda.synchronize()
             t1, t2 = [], []
-            for i in range(args.steps):
+            for i in range(steps):
                 flush_l2(flush, i)
                 ev[0].record()
                 run()
@@ -417,16 +537,60 @@ def sweep_main(args, synth, torch, moe):
             flop = 2.0 * live * (2 * I * H + H * I)
             wbytes = n_live_exp * (2 * I * H + H * I) * 2
             abytes = live * (H + 2 * I) * 2 + M * H * 2
+            t = (g1 + g2) * 1e-3
             rows.append({"live": live, "layout": layout, "experts_live": n_live_exp, "gate_up_ms": g1,
-                         "down_ms": g2, "pair_ms": g1 + g2, "pair_tflops": flop / ((g1 + g2) * 1e-3) / 1e12,
-                         "pair_hbm_gbs": (wbytes + abytes) / ((g1 + g2) * 1e-3) / 1e9,
+                         "down_ms": g2, "pair_ms": g1 + g2, "pair_tflops": flop / t / 1e12,
+                         "tensor_frac": flop / t / 1e12 / pk["bf16_tflops"],
+                         "pair_hbm_gbs": (wbytes + abytes) / t / 1e9,
+                         "hbm_frac": (wbytes + abytes) / t / 1e9 / pk["hbm_gbs"],
                          "hbm_roofline_ms": (wbytes + abytes) / (pk["hbm_gbs"] * 1e9) * 1e3,
                          "tensor_roofline_ms": flop / (pk["bf16_tflops"] * 1e12) * 1e3})
     full = {r["layout"]: r["pair_ms"] for r in rows if r["live"] == 16384}
     for r in rows:
         r["time_vs_full"] = r["pair_ms"] / full[r["layout"]]
+    del W1, W2, h, y2, flush
+    torch.cuda.empty_cache()
+    return rows
+
+
+def sweep_cpu_baseline(synth):
+    """The oracle's grouped GEMM pair (gate_up, silu * up, bf16 h, down) on
+    sampled live rows of the 2048-live sweep: rows/s on every core (OpenMP
+    build) and on one core."""
+    import oracle
+    sw = synth.Sweep(live=2048)
+    wl = sw.workload
+    A, off = synth.sweep_rows(sw), synth.sweep_offsets(sw)
+    W1, W2 = synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    cores, model = cpu_info()
+    res = {}
+    prev = oracle.use_openmp(True)
+    try:
+        for label, omp, n in (("all", True, 2048), ("one", False, 128)):
+            oracle.use_openmp(omp)
+            rows = np.linspace(0, sw.live - 1, n).astype(np.int32)
+            t0 = time.perf_counter()
+            hb = np.zeros((sw.M_cap, sw.I), np.uint16)
+            hb[rows] = oracle.bf16_round(oracle.swiglu(oracle.grouped_gemm_bf16(A, W1, off, rows=rows), n))
+            oracle.grouped_gemm_bf16(hb, W2, off, rows=rows)
+            dt = time.perf_counter() - t0
+            res[label] = (n / dt, n, dt, oracle.threads())
+    finally:
+        oracle.use_openmp(prev)
+    v, n, dt, thr = res["all"]
+    v1, n1, dt1, _ = res["one"]
+    return {"value": v, "unit": "rows/s", "cores": thr, "kind": "oracle",
+            "sample": f"{n} of the 2048 live rows ({dt:.1f} s), OpenMP build over rows on {thr} threads",
+            "single_core": {"value": v1, "unit": "rows/s", "cores": 1,
+                            "sample": f"{n1} live rows ({dt1:.1f} s), one-core build"},
+            "cpu": model, "host_cores": cores}
+
+
+def sweep_main(args, synth, torch, moe):
+    pk, pk_kind = peaks()
+    rows = sweep_measure(args.steps, args.warmup, synth, torch, moe, pk)
     print(json.dumps({"metric": "grouped GEMM pair time vs live rows (sentinel sweep)", "unit": "ms",
-                      "config": {"workload": "sweep-128e-h2048-i768-m16384", "dtype": "bf16",
+                      "config": {"workload": SWEEP_NAME, "dtype": "bf16",
                                  "l2": "flushed between steps", "steps": args.steps},
                       "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"], "kind": pk_kind},
                       "rows": rows}))
@@ -506,6 +670,98 @@ def grad_main(args, wl, synth, torch, moe):
     return 0
 
 
+# ------------------------------------------------------------------ timing
+def prepare_step(step, args, torch, moe):
+    """W warm-up steps, then (unless --no-graph) the step's C-ABI calls
+    captured once into a CUDA graph and replayed, as a serving loop would, so
+    that host launch gaps between its short kernels stay out of the step time.
+    Returns (run_step, graph or None)."""
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit(f"device error during warm-up ({step.wl.name})")
+    if args.no_graph:
+        return step.run, None
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step.run()                        # one eager pass on the capture stream
+        with torch.cuda.graph(graph, stream=side):
+            step.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit(f"device error in the captured step ({step.wl.name})")
+    return graph.replay, graph
+
+
+def timed_steps(run_step, step, flush, steps, torch):
+    """K steps timed with CUDA events on the launching stream, L2 flushed
+    (untimed) before each; then K eager steps with events between the kernels
+    for the per-kernel durations.  Returns (step_ms, wall seconds of the
+    first loop)."""
+    step_ms = []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush_l2(flush, i)
+        s0.record()
+        run_step()
+        s1.record()
+        torch.cuda.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+    wall = time.perf_counter() - wall0
+    for i in range(steps):
+        flush_l2(flush, i)
+        step.run(record=True)
+        torch.cuda.synchronize()
+        step.collect()
+    return step_ms, wall
+
+
+def preroll(run_step, torch, seconds):
+    """Untimed steps so that the 200 ms clock samples see the GPU under this load."""
+    t_pre = time.perf_counter()
+    while time.perf_counter() - t_pre < seconds:
+        run_step()
+        torch.cuda.synchronize()
+
+
+# the other workloads measured in the same run, beside the headline one
+CONFIG_WORKLOADS = ("tiny-8e-top2", "128e-top8-h2048-zipf", "256e-top8-h7168-fp8")
+
+
+def measure_config(wl, args, torch, moe, synth, pk, flush, device_index):
+    """One more layer workload with the headline's protocol (graph replay, L2
+    flushed between timed steps, per-kernel events), its CPU baseline beside
+    it; its buffers are freed before returning."""
+    L = make_layer(wl, torch, moe, synth)
+    step = Step(wl, L, torch, moe)
+    run_step, graph = prepare_step(step, args, torch, moe)
+    with ClockSampler(device_index) as clk:
+        preroll(run_step, torch, 0.3)
+        step_ms, wall = timed_steps(run_step, step, flush, args.steps, torch)
+    if moe.moe_get_device_error() != 0:
+        raise SystemExit(f"device error in the timed steps of {wl.name}")
+    rec = layer_summary(wl, step, step_ms, True, pk)
+    rec.pop("_fb")
+    rec["config"] = {"T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I, "dtype": wl.dtype,
+                     "bias": wl.bias, "sentinel_slots": wl.n_sentinel}
+    rec["steps"] = args.steps
+    rec["setup_s"] = L["setup_s"]
+    rec["clocks"] = clk.summary()
+    del graph, run_step, step, L
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline_record(wl, synth)
+    return rec
+
+
 # ------------------------------------------------------------------ main
 def main():
     args = parse()
@@ -559,61 +815,15 @@ def main():
                           "steps": args.warmup + args.steps, "device_error": err}))
         return 1 if err else 0
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    for i in range(max(3, args.warmup)):
-        step.run()
-    torch.cuda.synchronize()
-    if moe.moe_get_device_error() != 0:
-        raise SystemExit("device error during warm-up")
-    # The step's C-ABI calls are captured once into a CUDA graph and replayed,
-    # as a serving loop would, so that host launch gaps between its short
-    # kernels stay out of the step time.
-    run_step = step.run
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            step.run()                        # one eager pass on the capture stream
-            with torch.cuda.graph(graph, stream=side):
-                step.run()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        run_step = graph.replay
-        for _ in range(max(3, args.warmup)):
-            graph.replay()
-        torch.cuda.synchronize()
-        if moe.moe_get_device_error() != 0:
-            raise SystemExit("device error in the captured step")
+    run_step, graph = prepare_step(step, args, torch, moe)
 
     # ---- timed region: K steps, L2 flushed between steps (untimed)
     barrier()
     torch.cuda.synchronize()
-    step_ms = []
     with ClockSampler(local) as clk:
-        # untimed pre-roll (about 1 s) so that the 200 ms clock samples cover
-        # the GPU under this load, then the timed steps
-        t_pre = time.perf_counter()
-        while time.perf_counter() - t_pre < 1.0:
-            run_step()
-            torch.cuda.synchronize()
+        preroll(run_step, torch, 1.0)
         barrier()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush_l2(flush, i)
-            s0.record()
-            run_step()
-            s1.record()
-            torch.cuda.synchronize()
-            step_ms.append(s0.elapsed_time(s1))
-        wall = time.perf_counter() - wall0
-        # per-kernel durations: K more steps launched eagerly with CUDA events
-        # between the kernels on the launching stream
-        for i in range(args.steps):
-            flush_l2(flush, i)
-            step.run(record=True)
-            torch.cuda.synchronize()
-            step.collect()
+        step_ms, wall = timed_steps(run_step, step, flush, args.steps, torch)
     torch.cuda.synchronize()
     barrier()
     if moe.moe_get_device_error() != 0:
@@ -629,6 +839,7 @@ def main():
     fa = moe.forward_args(dtype=fa_dtype, T=wl.T, E=wl.E,
                           k=wl.k, H=wl.H, I=wl.I, x=x_pin, W1=L["w1"], W2=L["w2"], W1_scales=L.get("w1_s"),
                           W2_scales=L.get("w2_s"), out=out_pin, logits=lg_pin, expert_bias=L["bias"],
+                          sentinel_mask=L["mask"],
                           renormalize=wl.renormalize, host_io=True, gather=not separate)
     nws = moe.moe_forward_workspace_size(fa)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
@@ -661,7 +872,8 @@ def main():
     outs_pin = [torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory() for _ in range(2)]
     fa_dev = [moe.forward_args(dtype=fa_dtype, T=wl.T, E=wl.E, k=wl.k, H=wl.H, I=wl.I, x=d_x[i],
                                W1=L["w1"], W2=L["w2"], W1_scales=L.get("w1_s"), W2_scales=L.get("w2_s"),
-                               out=d_out[i], logits=d_lg[i], expert_bias=L["bias"], renormalize=wl.renormalize,
+                               out=d_out[i], logits=d_lg[i], expert_bias=L["bias"], sentinel_mask=L["mask"],
+                               renormalize=wl.renormalize,
                                gather=not separate) for i in range(2)]
     s_comp, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in_ready", "in_free", "out_ready", "out_free")}
@@ -721,42 +933,54 @@ def main():
         return 0
 
     # ---- roofline of the dominant kernel (the gate_up grouped GEMM)
-    off = step.off.cpu().numpy()
-    live = int(off[-1])
-    experts_live = int((np.diff(off) > 0).sum())
-    fb = flops_bytes(wl, live, experts_live, separate)
-    kt = {n: statistics.fmean(v) for n, v in step.times.items()}
     pk, pk_kind = peaks()
-    g1 = kt["gemm_gate_up_swiglu"]
-    g2 = kt["gemm_down"]
-    if wl.dtype == "fp8":
-        peak = pk["bf16_tflops"] * 2.0        # fp8 dense = 2 x bf16 (nominal ratio)
-        peak_note = f"fp8 = 2 x {pk_kind} bf16 burst"
-    else:
-        peak = pk["bf16_tflops"]
-        peak_note = f"{pk_kind} bf16 burst (cuBLAS)"
-    ach1 = fb["gemm1_flop"] / (g1 * 1e-3) / 1e12
-    ach2 = fb["gemm2_flop"] / (g2 * 1e-3) / 1e12
+    summ = layer_summary(wl, step, step_ms, separate, pk)
+    fb = summ.pop("_fb")
+    live, experts_live = summ["live_rows"], summ["experts_with_rows"]
+    g = summ["gemm"]["gate_up"]
+    fp8 = wl.dtype == "fp8"
+    peak_note = (f"fp8 = 2 x {pk_kind} bf16 burst" if fp8 else f"{pk_kind} bf16 burst (cuBLAS)")
     traffic = None
     tp = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
     if os.path.exists(tp):
         with open(tp) as f:
             traffic = json.load(f).get("gemm_gate_up_swiglu_bytes" if separate
                                        else "gemm_gate_up_swiglu_gather_bytes")
-    cores, model = cpu_info()
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        W1, W2, s1, s2 = host_weights(wl, synth)
-        n = args.cpu_sample_tokens if wl.dtype != "fp8" else max(1, args.cpu_sample_tokens // 8)
-        v, dt = oracle_tokens_per_s(wl, n, L["x_host"], L["logits_host"], L["bias_host"], W1, W2, s1, s2)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {n} of {wl.T} tokens of {wl.name} ({dt:.1f} s)", "cpu": model,
-               "host_cores": cores}
+    kernel_name = ("grouped GEMM gate_up + fused SwiGLU" + (" + FP8 quantisation of h" if fp8 else "")
+                   if separate else "grouped GEMM gate_up, A gathered from token order, + fused SwiGLU")
+    if fb["gemm1_bytes"] / (pk["hbm_gbs"] * 1e9) > fb["gemm1_flop"] / (summ["peaks"]["tensor_tflops"] * 1e12):
+        roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": g["hbm_gbs"], "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": g["hbm_frac"], "peak_source": f"{pk_kind} HBM copy bandwidth",
+                    "traffic": traffic, "tensor_frac": g["tensor_frac"], "tensor_peak_source": peak_note}
+    else:
+        roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": g["tflops"],
+                    "peak": summ["peaks"]["tensor_tflops"], "unit": "TFLOP/s", "frac": g["tensor_frac"],
+                    "peak_source": peak_note, "traffic": traffic}
+    roofline.update(algorithmic_flop=fb["gemm1_flop"], algorithmic_bytes=fb["gemm1_bytes"])
     clocks = clk.summary()
+    cpu = None
+    configs = None
+    if world == 1:
+        if not args.no_cpu_baseline:
+            cpu = cpu_baseline_record(wl, synth)
+        if not args.no_configs:
+            # the other workloads, each with its own CPU baseline; these run
+            # after the timed region above and are not part of its steps
+            configs = {}
+            for name in CONFIG_WORKLOADS:
+                if name != wl.name:
+                    configs[name] = measure_config(synth.WORKLOADS[name], args, torch, moe, synth, pk, flush,
+                                                   local)
+            with ClockSampler(local) as sclk:
+                rows = sweep_measure(args.steps, args.warmup, synth, torch, moe, pk)
+            configs[SWEEP_NAME] = {"rows": rows, "steps": args.steps, "clocks": sclk.summary(),
+                                   "l2": "flushed between steps"}
+            if not args.no_cpu_baseline:
+                configs[SWEEP_NAME]["cpu_baseline"] = sweep_cpu_baseline(synth)
     line = {
         "metric": METRIC, "value": job_tokens_per_s(wl.T, world, ms_max), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if wl.dtype == "fp8" else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded numpy draws; random-init weights N(0,0.02))",
         "config": {"workload": wl.name, "T": wl.T, "E": wl.E, "k": wl.k, "H": wl.H, "I": wl.I,
                    "bias": wl.bias, "live_rows": live, "experts_with_rows": experts_live,
@@ -764,20 +988,18 @@ def main():
                    "scatter": "separate kernel" if separate else "gathered inside the gate_up GEMM",
                    "l2": "flushed between timed steps (256 MiB write, then read back; untimed)",
                    "launch": "eager C-ABI calls" if args.no_graph else "CUDA graph of the step's C-ABI calls"},
-        "roofline": {"bound": "tensor",
-                     "kernel": ("grouped GEMM gate_up + fused SwiGLU" if separate else
-                                "grouped GEMM gate_up, A gathered from token order, + fused SwiGLU"),
-                     "achieved": ach1, "peak": peak, "unit": "TFLOP/s", "frac": ach1 / peak,
-                     "peak_source": peak_note, "traffic": traffic,
-                     "algorithmic_flop": fb["gemm1_flop"], "algorithmic_bytes": fb["gemm1_bytes"]},
-        "gemm": {"gate_up_tflops": ach1, "down_tflops": ach2, "gate_up_frac": ach1 / peak,
-                 "down_frac": ach2 / peak,
-                 "pair_tflops": (fb["gemm1_flop"] + fb["gemm2_flop"]) / ((g1 + g2) * 1e-3) / 1e12},
-        "kernels_ms": kt,
-        "hbm": {"permute_gbs": (fb["permute_bytes"] / (kt["permute"] * 1e-3) / 1e9 if "permute" in kt
-                                else None),
-                "combine_gbs": fb["combine_bytes"] / (kt["combine"] * 1e-3) / 1e9,
-                "peak_gbs": pk["hbm_gbs"]},
+        "roofline": roofline,
+        "gemm": {"gate_up_tflops": summ["gemm"]["gate_up"]["tflops"],
+                 "down_tflops": summ["gemm"]["down"]["tflops"],
+                 "gate_up_frac": summ["gemm"]["gate_up"]["tensor_frac"],
+                 "down_frac": summ["gemm"]["down"]["tensor_frac"],
+                 "pair_tflops": (fb["gemm1_flop"] + fb["gemm2_flop"]) /
+                 ((summ["kernels_ms"]["gemm_gate_up_swiglu"] + summ["kernels_ms"]["gemm_down"]) * 1e-3) / 1e12,
+                 "detail": summ["gemm"]},
+        "kernels_ms": summ["kernels_ms"],
+        "hbm": {"permute_gbs": summ["data_movement"].get("permute", {}).get("gbs"),
+                "combine_gbs": summ["data_movement"]["combine"]["gbs"],
+                "peak_gbs": pk["hbm_gbs"], "detail": summ["data_movement"]},
         "e2e": {"value": job_tokens_per_s(wl.T, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2,
@@ -791,6 +1013,7 @@ def main():
         "gpu_launches": step.launches_per_step() * args.steps * 2,   # graph replays + eager steps
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "configs": configs,
         "wall_s_timed": wall,
         "setup_s": L["setup_s"],
     }
