@@ -210,6 +210,22 @@ void orc_sort_by_expert(const int32_t* ids, int64_t R, int E, int32_t* sorted_ro
     for (int e = 0; e < E; ++e) offsets[e + 1] = static_cast<int32_t>(offsets[e] + cnt[e]);
 }
 
+// Expert parallelism ("Mixture of Experts in transformers", expert
+// parallelism): the experts are sharded on their first dimension, rank r
+// holding the global experts [first, first + E_local); a router pick of a
+// local expert becomes its local id (id - first), any other pick -- another
+// rank's expert, or the global sentinel E_global -- becomes the local
+// sentinel E_local, so the local layer leaves it out (section 2 of the
+// transformers MoE/FP8 write-up).  An id outside [0, E_global] is not a pick
+// at all and becomes the sentinel too.
+void orc_ep_local_ids(const int32_t* ids, int64_t R, int E_global, int first, int E_local,
+                      int32_t* local_ids) {
+    for (int64_t i = 0; i < R; ++i) {
+        const int32_t id = ids[i];
+        local_ids[i] = (id >= first && id < first + E_local && id < E_global) ? id - first : E_local;
+    }
+}
+
 // ---------------------------------------------------------------- FP8 quant
 // Per-token activation quantisation (fp8_act_quant / per_token_cast_to_fp8
 // of section 1): for row m and 128-column group g,

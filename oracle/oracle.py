@@ -19,7 +19,7 @@ _LIBS = {False: os.path.join(_HERE, "libmoe_oracle.so"),       # one core
 
 __all__ = [
     "build", "use_openmp", "threads", "e4m3_encode", "e4m3_decode", "bf16_round", "route_topk",
-    "mark_sentinels", "sort_by_expert", "quant_act_fp8", "quant_weight_fp8", "permute",
+    "mark_sentinels", "ep_local_ids", "sort_by_expert", "quant_act_fp8", "quant_weight_fp8", "permute",
     "grouped_gemm_bf16", "grouped_gemm_fp8", "swiglu", "combine", "moe_forward",
     "grouped_gemm_dgrad_bf16", "grouped_gemm_wgrad_bf16",
 ]
@@ -106,6 +106,15 @@ def mark_sentinels(ids, mask, E: int):
     mask = _c(mask, np.uint8)
     _L().orc_mark_sentinels(_p(ids), _p(mask), C.c_int64(ids.size), E)
     return ids
+
+
+def ep_local_ids(ids, E_global: int, first: int, E_local: int):
+    """Global expert ids -> the ids of the rank holding experts [first,
+    first + E_local); every other pick becomes the local sentinel E_local."""
+    ids = _c(ids, np.int32)
+    out = np.empty(ids.shape, np.int32)
+    _L().orc_ep_local_ids(_p(ids), C.c_int64(ids.size), E_global, first, E_local, _p(out))
+    return out
 
 
 def sort_by_expert(ids, E: int):
