@@ -50,6 +50,7 @@ _SIGS = {
     "moe_route_sort_workspace_size": (_Z, [_I, _I, _I]),
     "moe_route_sort": (_S, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_route_sort_noalloc": (_S, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_ep_local_ids": (_S, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_act_quant_fp8": (_S, [_P, _I, _I, _P, _P, _P]),
     "moe_weight_quant_fp8": (_S, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_S, [_I, _P, _P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P]),
@@ -152,6 +153,11 @@ def moe_route_sort_noalloc(logits, expert_bias, sentinel_mask, topk_ids, topk_w,
                                         _p(topk_w), T, E, k, int(renormalize), _p(sorted_rows),
                                         _p(row_pos), _p(offsets), _stream(stream)),
            "moe_route_sort_noalloc")
+
+
+def moe_ep_local_ids(topk_ids, T, k, E_global, first_expert, E_local, local_ids, stream=None):
+    _check(lib().moe_ep_local_ids(_p(topk_ids), T, k, E_global, first_expert, E_local, _p(local_ids),
+                                  _stream(stream)), "moe_ep_local_ids")
 
 
 def moe_act_quant_fp8(x, M, K, q, scales, stream=None):

@@ -183,6 +183,29 @@ moe_status_t moe_route_sort_noalloc(const float* logits, const float* expert_bia
                                     moe_stream_t stream);
 
 /*
+ * moe_ep_local_ids -- the router side of expert parallelism ("Mixture of
+ * Experts in transformers", section on expert parallelism: the stacked
+ * expert weights are sharded on their first dimension, and the router's
+ * global expert ids are remapped to each rank's local ids, the picks of other
+ * ranks' experts being masked; the ranks' partial outputs are then summed by
+ * an all-reduce).  For the rank holding global experts [first_expert,
+ * first_expert + E_local):
+ *   local_ids[f] = topk_ids[f] - first_expert  if that expert is local,
+ *                  E_local (the local sentinel) otherwise,
+ * for every slot f < T*k.  The global sentinel E_global maps to E_local; an id
+ * outside [0, E_global] is recorded as MOE_DEVERR_ROUTE and maps to E_local.
+ * local_ids then feeds moe_route_sort (logits NULL, E = E_local) or
+ * moe_forward (logits NULL, topk_ids = local_ids, topk_w = the global
+ * weights, the rank's own W1/W2 slices, E = E_local); summing the ranks'
+ * outputs gives the unsharded layer (the combine is linear in the experts).
+ * topk_ids and local_ids int32 [T, k] (device; they may be the same buffer).
+ * Limits: 1 <= E_global <= 256, E_local >= 1, 0 <= first_expert,
+ * first_expert + E_local <= E_global, T*k < 2^31.
+ */
+moe_status_t moe_ep_local_ids(const int32_t* topk_ids, int T, int k, int E_global, int first_expert,
+                              int E_local, int32_t* local_ids, moe_stream_t stream);
+
+/*
  * moe_act_quant_fp8 -- per-token activation quantisation (fp8_act_quant /
  * per_token_cast_to_fp8 of section 1 of the transformers MoE/FP8 write-up).
  * For row m and 128-column group g: s = amax(|x[m, g*128 : g*128+128]|) / 448
