@@ -1009,7 +1009,9 @@ def main():
                          "); all copies inside the timed region"),
                 "batches": n_serve,
                 "serial_value": job_tokens_per_s(wl.T, world, e2e_serial_max),
-                "serial_mode": "moe_forward with MOE_FWD_HOST_IO: copy in, kernels, copy out back to back"},
+                "serial_mode": ("moe_forward with MOE_FWD_HOST_IO on pinned buffers, one batch at a time: "
+                                "the kernels read x and the logits and write the output in host memory "
+                                "over the host link")},
         "gpu_launches": step.launches_per_step() * args.steps * 2,   # graph replays + eager steps
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -5,7 +5,9 @@
 // weighted gather.  With MOE_FWD_GATHER the scatter is folded into the
 // gate_up GEMM, which then reads its rows from token order
 // (moe_grouped_gemm_gather) and no permuted copy of x is held.  Offsets stay
-// on the device; there is no host synchronisation.
+// on the device; there is no host synchronisation.  With MOE_FWD_HOST_IO,
+// pinned host buffers are read and written by the kernels in place; other
+// host memory is staged through the workspace.
 #include "common.cuh"
 
 namespace {
@@ -89,6 +91,19 @@ Layout layout(const moe_forward_args* a) {
     return l;
 }
 
+// The device address of a host buffer that the kernels may read or write in
+// place: page-locked (pinned) host memory mapped into the device's address
+// space.  NULL for any other host memory (pageable), which is staged through
+// the workspace with cudaMemcpyAsync instead.
+const void* mapped_host_view(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 #define MOE_TRY(call)                          \
     do {                                       \
         const moe_status_t st_ = (call);       \
@@ -118,17 +133,36 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
     const void* x = a->x;
     const float* logits = a->logits;
     void* out = a->out;
+    bool copy_out = false;
     if (host_io) {
-        void* xd = base + l.x_dev;
-        MOE_CHECK_CUDA(cudaMemcpyAsync(xd, a->x, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice, s));
-        x = xd;
-        if (logits) {
-            float* ld = reinterpret_cast<float*>(base + l.logits_dev);
-            MOE_CHECK_CUDA(cudaMemcpyAsync(ld, a->logits, static_cast<size_t>(T) * E * 4,
-                                           cudaMemcpyHostToDevice, s));
-            logits = ld;
+        // Pinned buffers are read and written in place by the kernels (the
+        // routing reads the logits, the quantiser or the permute reads x, the
+        // combine writes out) over the host link, with no staging copy and no
+        // copy engine between them and the layer.  Other host memory is
+        // staged through the workspace.
+        if (const void* xv = mapped_host_view(a->x)) {
+            x = xv;
+        } else {
+            void* xd = base + l.x_dev;
+            MOE_CHECK_CUDA(cudaMemcpyAsync(xd, a->x, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice, s));
+            x = xd;
         }
-        out = base + l.out_dev;
+        if (logits) {
+            if (const void* lv = mapped_host_view(logits)) {
+                logits = static_cast<const float*>(lv);
+            } else {
+                float* ld = reinterpret_cast<float*>(base + l.logits_dev);
+                MOE_CHECK_CUDA(cudaMemcpyAsync(ld, a->logits, static_cast<size_t>(T) * E * 4,
+                                               cudaMemcpyHostToDevice, s));
+                logits = ld;
+            }
+        }
+        if (const void* ov = mapped_host_view(a->out)) {
+            out = const_cast<void*>(ov);
+        } else {
+            out = base + l.out_dev;
+            copy_out = true;
+        }
     }
     int32_t* ids = a->topk_ids ? a->topk_ids : reinterpret_cast<int32_t*>(base + l.ids);
     float* w = a->topk_w ? a->topk_w : reinterpret_cast<float*>(base + l.w);
@@ -173,7 +207,7 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
                                  MOE_EPI_STORE, y2, nullptr, stream));
     }
     MOE_TRY(moe_combine(y2, ids, w, row_pos, T, k, H, E, out, stream));
-    if (host_io)
+    if (copy_out)
         MOE_CHECK_CUDA(cudaMemcpyAsync(a->out, out, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost, s));
     return MOE_OK;
 }

@@ -355,9 +355,15 @@ moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* t
                          moe_stream_t stream);
 
 /* moe_forward flags */
-#define MOE_FWD_HOST_IO 1u /* x, logits and out are HOST pointers (pinned memory
-                              recommended); the call stages them through the
-                              workspace with cudaMemcpyAsync on `stream` */
+#define MOE_FWD_HOST_IO 1u /* x, logits and out are HOST pointers.  Pinned
+                              (page-locked, mapped) buffers are read and
+                              written in place by the kernels over the host
+                              link (the routing reads logits, the quantiser or
+                              permute reads x, the combine writes out), with
+                              no staging copy; other host memory is staged
+                              through the workspace with cudaMemcpyAsync on
+                              `stream`.  Either way the results equal the
+                              device-buffer call's bit for bit. */
 #define MOE_FWD_GATHER 2u  /* fold the scatter into the gate_up GEMM
                               (moe_grouped_gemm_gather instead of moe_permute
                               + moe_grouped_gemm): same results, bit for bit,

@@ -39,9 +39,12 @@ def run_forward(moe, wl, x, W1, W2, W1s=None, W2s=None, host_io=False, logits=No
     ids = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
     if host_io:
-        xin = torch.from_numpy(x.view(np.int16)).pin_memory()
-        lin = torch.from_numpy(logits).pin_memory()
-        out = torch.empty((T, H), dtype=torch.int16).pin_memory()
+        # pinned buffers are read and written in place by the kernels;
+        # pageable ones are staged through the workspace by the library
+        pin = (lambda t: t.pin_memory()) if host_io != "pageable" else (lambda t: t.clone())
+        xin = pin(torch.from_numpy(x.view(np.int16)))
+        lin = pin(torch.from_numpy(logits))
+        out = pin(torch.empty((T, H), dtype=torch.int16))
     else:
         xin, lin = dev_bf16(x), dev(logits)
         out = torch.empty((T, H), dtype=torch.int16, device="cuda")
@@ -49,7 +52,7 @@ def run_forward(moe, wl, x, W1, W2, W1s=None, W2s=None, host_io=False, logits=No
                          I=wl.I, x=xin, W1=W1, W2=W2, W1_scales=W1s, W2_scales=W2s, out=out, logits=lin,
                          expert_bias=None if bias is None else dev(bias),
                          sentinel_mask=None if mask is None else dev(mask), topk_ids=ids, topk_w=w,
-                         renormalize=wl.renormalize, host_io=host_io)
+                         renormalize=wl.renormalize, host_io=bool(host_io))
     nbytes = moe.moe_forward_workspace_size(a)
     assert nbytes > 0
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
@@ -98,16 +101,30 @@ def test_forward_fp8(moe, wl):
     assert err.max() <= TOL["fp8"], err.max()
 
 
-def test_forward_host_io_equals_device_path(moe):
+@pytest.mark.parametrize("memory", ["pinned", "pageable"])
+def test_forward_host_io_equals_device_path(moe, memory):
     wl = LAYERS[1]
     x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
     logits = synth.router_logits(wl)
     d1, d2 = dev_bf16(W1), dev_bf16(W2)
     y_dev, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits)
-    y_host, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits, host_io=True)
+    y_host, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits, host_io=memory)
     assert np.array_equal(y_dev, y_host)
     y_again, _, _ = run_forward(moe, wl, x, d1, d2, logits=logits)
     assert np.array_equal(y_dev, y_again)                     # bit-reproducible
+
+
+@pytest.mark.parametrize("memory", ["pinned", "pageable"])
+def test_fp8_forward_host_io_equals_device_path(moe, memory):
+    wl = synth.Workload("fp8-host-io", T=150, E=8, k=2, H=256, I=256, n_sentinel=9, dtype="fp8")
+    x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
+    logits, mask = synth.router_logits(wl), synth.sentinel_mask(wl)
+    q1, s1 = oracle.quant_weight_fp8(W1)
+    q2, s2 = oracle.quant_weight_fp8(W2)
+    w = (dev(q1), dev(q2), dev(s1), dev(s2))
+    y_dev, _, _ = run_forward(moe, wl, x, w[0], w[1], w[2], w[3], logits=logits, mask=mask)
+    y_host, _, _ = run_forward(moe, wl, x, w[0], w[1], w[2], w[3], logits=logits, mask=mask, host_io=memory)
+    assert np.array_equal(y_dev, y_host)
 
 
 def test_expert_parallel_shards_on_one_gpu(moe):
