@@ -5,9 +5,11 @@
 // weighted gather.  With MOE_FWD_GATHER the scatter is folded into the
 // gate_up GEMM, which then reads its rows from token order
 // (moe_grouped_gemm_gather) and no permuted copy of x is held.  Offsets stay
-// on the device; there is no host synchronisation.  With MOE_FWD_HOST_IO,
-// pinned host buffers are read and written by the kernels in place; other
-// host memory is staged through the workspace.
+// on the device; there is no host synchronisation.  With MOE_FWD_HOST_IO, x
+// is copied in on a second stream while the batch is routed, and a pinned
+// output buffer is written in place by the combine.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -91,17 +93,49 @@ Layout layout(const moe_forward_args* a) {
     return l;
 }
 
-// The device address of a host buffer that the kernels may read or write in
-// place: page-locked (pinned) host memory mapped into the device's address
-// space.  NULL for any other host memory (pageable), which is staged through
-// the workspace with cudaMemcpyAsync instead.
-const void* mapped_host_view(const void* p) {
+// The device address of pinned (page-locked, mapped) host memory, which a
+// kernel may write in place; NULL for pageable host memory.
+void* mapped_host_view(const void* p) {
     cudaPointerAttributes at{};
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return nullptr;
     }
     return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// A second stream per device for the host-to-device copy of x, with the two
+// events that fork it from and join it to the caller's stream.  Created on
+// first use and kept for the life of the process; the mutex keeps the
+// record/wait sequences of concurrent calls from interleaving.
+struct CopyStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, ready = nullptr;
+    std::mutex mu;
+};
+constexpr int kMaxDevices = 64;
+CopyStream g_copy[kMaxDevices];
+std::mutex g_copy_init;
+
+CopyStream* copy_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    CopyStream& c = g_copy[dev];
+    std::lock_guard<std::mutex> lk(g_copy_init);
+    if (!c.stream) {
+        cudaStream_t st = nullptr;
+        cudaEvent_t a = nullptr, b = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        c.fork = a;
+        c.ready = b;
+        c.stream = st;
+    }
+    return &c;
 }
 
 #define MOE_TRY(call)                          \
@@ -134,31 +168,34 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
     const float* logits = a->logits;
     void* out = a->out;
     bool copy_out = false;
+    CopyStream* cs = nullptr;
+    std::unique_lock<std::mutex> cs_lock;
     if (host_io) {
-        // Pinned buffers are read and written in place by the kernels (the
-        // routing reads the logits, the quantiser or the permute reads x, the
-        // combine writes out) over the host link, with no staging copy and no
-        // copy engine between them and the layer.  Other host memory is
-        // staged through the workspace.
-        if (const void* xv = mapped_host_view(a->x)) {
-            x = xv;
-        } else {
-            void* xd = base + l.x_dev;
-            MOE_CHECK_CUDA(cudaMemcpyAsync(xd, a->x, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice, s));
-            x = xd;
-        }
+        // x (the large input) is copied in on a second stream while the
+        // logits are copied and the batch routed on `stream`; the caller's
+        // stream waits for x before the first kernel that reads it.  The
+        // output of a pinned `out` is written in place by the combine;
+        // pageable output memory gets a staged copy.  (Kernels reading pinned
+        // inputs over the host link in place were slower than the copy
+        // engine; writing the output in place was faster than a copy.)
+        cs = copy_stream();
+        if (!cs) return MOE_ERR_CUDA;
+        cs_lock = std::unique_lock<std::mutex>(cs->mu);
+        void* xd = base + l.x_dev;
+        MOE_CHECK_CUDA(cudaEventRecord(cs->fork, s));   // earlier users of the staging buffer are done
+        MOE_CHECK_CUDA(cudaStreamWaitEvent(cs->stream, cs->fork, 0));
+        MOE_CHECK_CUDA(cudaMemcpyAsync(xd, a->x, static_cast<size_t>(T) * H * 2, cudaMemcpyHostToDevice,
+                                       cs->stream));
+        MOE_CHECK_CUDA(cudaEventRecord(cs->ready, cs->stream));
+        x = xd;
         if (logits) {
-            if (const void* lv = mapped_host_view(logits)) {
-                logits = static_cast<const float*>(lv);
-            } else {
-                float* ld = reinterpret_cast<float*>(base + l.logits_dev);
-                MOE_CHECK_CUDA(cudaMemcpyAsync(ld, a->logits, static_cast<size_t>(T) * E * 4,
-                                               cudaMemcpyHostToDevice, s));
-                logits = ld;
-            }
+            float* ld = reinterpret_cast<float*>(base + l.logits_dev);
+            MOE_CHECK_CUDA(cudaMemcpyAsync(ld, a->logits, static_cast<size_t>(T) * E * 4,
+                                           cudaMemcpyHostToDevice, s));
+            logits = ld;
         }
-        if (const void* ov = mapped_host_view(a->out)) {
-            out = const_cast<void*>(ov);
+        if (void* ov = mapped_host_view(a->out)) {
+            out = ov;
         } else {
             out = base + l.out_dev;
             copy_out = true;
@@ -173,6 +210,10 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
     MOE_TRY(moe_route_sort(logits, a->expert_bias, a->sentinel_mask, ids, w, T, E, k, a->renormalize,
                            sorted_rows, row_pos, offsets, base + l.route,
                            moe_route_sort_workspace_size(T, E, k), stream));
+    if (cs) {   // x has arrived before anything reads it
+        MOE_CHECK_CUDA(cudaStreamWaitEvent(s, cs->ready, 0));
+        cs_lock.unlock();
+    }
     void* y2 = base + l.y2;
     if (!fp8) {
         void* h = base + l.h;

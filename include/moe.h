@@ -257,6 +257,8 @@ moe_status_t moe_permute(moe_dtype_t dtype, const void* x, const float* x_scales
  *
  * A        bf16 [M_cap, K], or e4m3 [M_cap, K] with A_scales fp32 [K/128, M_cap]
  * B        bf16 [E, N, K], or e4m3 [E, N, K] with B_scales fp32 [E, ceil(N/128), K/128]
+ *          (B_scales need only be 4-byte aligned, so that a run of experts
+ *          sliced out of a larger stack can be passed as it is)
  * offsets  int32 [E+1] (device).
  * epilogue MOE_EPI_STORE:  C bf16 [M_cap, N]
  *          MOE_EPI_SWIGLU: rows [0, N/2) of B[e] are the gate, [N/2, N) the
@@ -355,15 +357,18 @@ moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* t
                          moe_stream_t stream);
 
 /* moe_forward flags */
-#define MOE_FWD_HOST_IO 1u /* x, logits and out are HOST pointers.  Pinned
-                              (page-locked, mapped) buffers are read and
-                              written in place by the kernels over the host
-                              link (the routing reads logits, the quantiser or
-                              permute reads x, the combine writes out), with
-                              no staging copy; other host memory is staged
-                              through the workspace with cudaMemcpyAsync on
-                              `stream`.  Either way the results equal the
-                              device-buffer call's bit for bit. */
+#define MOE_FWD_HOST_IO 1u /* x, logits and out are HOST pointers (pinned memory
+                              recommended).  x and logits are staged through
+                              the workspace with cudaMemcpyAsync: x on a
+                              second stream owned by the library (one per
+                              device, created on the first such call), so the
+                              routing on `stream` overlaps its copy; `stream`
+                              waits for it before x is read.  A pinned `out`
+                              is written in place by the combine kernel;
+                              pageable `out` gets a staged copy back.  The
+                              results equal the device-buffer call's bit for
+                              bit.  Calls made under stream capture take the
+                              library's copy stream into the capture. */
 #define MOE_FWD_GATHER 2u  /* fold the scatter into the gate_up GEMM
                               (moe_grouped_gemm_gather instead of moe_permute
                               + moe_grouped_gemm): same results, bit for bit,
@@ -393,9 +398,9 @@ typedef struct {
     float* topk_w;                /* [T, k] (device); NULL likewise */
     const void* x;                /* bf16 [T, H] */
     const void* W1;               /* bf16 or e4m3 [E, 2I, H] (device) */
-    const float* W1_scales;       /* FP8: [E, 2I/128, H/128] (device) */
+    const float* W1_scales;       /* FP8: [E, 2I/128, H/128] (device; 4-byte aligned) */
     const void* W2;               /* bf16 or e4m3 [E, H, I] (device) */
-    const float* W2_scales;       /* FP8: [E, ceil(H/128), I/128] (device) */
+    const float* W2_scales;       /* FP8: [E, ceil(H/128), I/128] (device; 4-byte aligned) */
     void* out;                    /* bf16 [T, H] */
 } moe_forward_args;
 

@@ -215,3 +215,68 @@ def test_fp8_token_tile_boundaries(moe, epi):
         assert np.array_equal(host(hq)[:live], host(q2)[:live])
         assert np.array_equal(host(hs).T[:live], host(s2)[:live])
         assert np.all(host(hq)[live:] == 0) and np.all(host(hs).T[live:] == 1.0)
+
+
+# FP8 with experts of several token tiles and a row buffer far larger than
+# the live rows: expert sizes around multiples of 128 and 256 (up to eight
+# row tiles), empty experts, all three epilogues; and the live rows'
+# results must not depend on M_cap.
+FP8_WIDE_COUNTS = [1, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 513, 0, 1000, 0, 0, 0, 0, 0]
+
+
+def _fp8_wide_case(epi, seed):
+    E = len(FP8_WIDE_COUNTS)
+    off = np.concatenate([[0], np.cumsum(FP8_WIDE_COUNTS)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap, K = 256 * E + 64, 384
+    assert M_cap >= live
+    N = 384 if epi == "store" else 2 * 256
+    A = synth.grouped_rows(M_cap, K, live, seed=seed)
+    A[live:] = 0
+    qa, sa = oracle.quant_act_fp8(A)
+    qb, sb = oracle.quant_weight_fp8(_weights(E, N, K, seed + 1))
+    return E, off, live, M_cap, N, K, qa, sa, qb, sb
+
+
+@pytest.mark.parametrize("epi", ["store", "swiglu", "swiglu_q"])
+def test_fp8_many_row_tiles(moe, epi):
+    E, off, live, M_cap, N, K, qa, sa, qb, sb = _fp8_wide_case(epi, 81)
+    ref = oracle.grouped_gemm_fp8(qa, sa, qb, sb, off)
+    args = (dev(qa), dev(np.ascontiguousarray(sa.T)), dev(qb), dev(sb), dev(off), E, M_cap, N, K)
+    if epi == "store":
+        C = torch.full((M_cap, N), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_STORE, C, None)
+        assert moe.moe_get_device_error() == 0
+        assert_close_bf16(host_f32_from_bf16(C)[:live], ref[:live], rtol=2.0 ** -7, row_atol=2e-3)
+        assert np.all(host_bf16_bits(C)[live:] == 0)
+        return
+    I = N // 2
+    ref_h = oracle.swiglu(ref, live)
+    h = torch.full((M_cap, I), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_SWIGLU, h, None)
+    assert moe.moe_get_device_error() == 0
+    assert_close_bf16(host_f32_from_bf16(h)[:live], ref_h[:live], rtol=2.0 ** -7, row_atol=2e-3)
+    assert np.all(host_bf16_bits(h)[live:] == 0)
+    if epi == "swiglu_q":
+        hq = torch.full((M_cap, I), 7, dtype=torch.uint8, device="cuda")
+        hs = torch.full((I // 128, M_cap), -1.0, dtype=torch.float32, device="cuda")
+        moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, *args, moe.MOE_EPI_SWIGLU_QUANT_FP8, hq, hs)
+        assert moe.moe_get_device_error() == 0
+        q2 = torch.empty((M_cap, I), dtype=torch.uint8, device="cuda")
+        s2 = torch.empty((M_cap, I // 128), dtype=torch.float32, device="cuda")
+        moe.moe_act_quant_fp8(h, M_cap, I, q2, s2)
+        assert np.array_equal(host(hq)[:live], host(q2)[:live])
+        assert np.array_equal(host(hs).T[:live], host(s2)[:live])
+        assert np.all(host(hq)[live:] == 0) and np.all(host(hs).T[live:] == 1.0)
+
+
+def test_fp8_live_rows_do_not_depend_on_m_cap(moe):
+    E, off, live, M_cap, N, K, qa, sa, qb, sb = _fp8_wide_case("store", 91)
+    outs = []
+    for m in (M_cap, live):
+        C = torch.empty((m, N), dtype=torch.bfloat16, device="cuda")
+        moe.moe_grouped_gemm(moe.MOE_FP8_E4M3_B128, dev(qa[:m]), dev(np.ascontiguousarray(sa[:m].T)), dev(qb),
+                             dev(sb), dev(off), E, m, N, K, moe.MOE_EPI_STORE, C, None)
+        assert moe.moe_get_device_error() == 0
+        outs.append(host_bf16_bits(C)[:live])
+    assert np.array_equal(outs[0], outs[1])
