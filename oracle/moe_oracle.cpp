@@ -416,6 +416,47 @@ void orc_grouped_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb,
     }
 }
 
+// Batched expert products (the batched_mm backend of "MoE in transformers"'s
+// pluggable expert backends; batched_fp8_matmul of section 1 of the
+// transformers write-up): for every slot f = t*k + j whose expert e =
+// ids[f] is not the sentinel E,
+//   out[f, n] = sum_c x[t, c] * W[e, n, c]
+// (bf16: exact widening, double accumulation; FP8: e4m3 with per-row scales
+// xs [T, K/128] and block scales Ws [E, ceil(N/128), K/128], the
+// block-scaled sum of orc_grouped_gemm_fp8); sentinel slots get zero rows.
+// out is fp32 [T*k, N].
+void orc_batched_matmul(int fp8, const void* x, const float* xs, const int32_t* ids, int64_t T, int k, int E,
+                        const void* W, const float* Ws, int N, int K, float* out) {
+    const int KB = K / 128, NB = (N + 127) / 128;
+    const float* dec = e4m3_table();
+    for (int64_t f = 0; f < T * k; ++f) {
+        const int64_t t = f / k;
+        const int e = ids[f];
+        float* o = out + f * N;
+        if (e < 0 || e >= E) {
+            for (int n = 0; n < N; ++n) o[n] = 0.0f;
+            continue;
+        }
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            if (!fp8) {
+                const uint16_t* xr = static_cast<const uint16_t*>(x) + t * K;
+                const uint16_t* wr = static_cast<const uint16_t*>(W) + ((int64_t)e * N + n) * K;
+                for (int c = 0; c < K; ++c) acc += (double)bf16_to_f32(xr[c]) * (double)bf16_to_f32(wr[c]);
+            } else {
+                const uint8_t* xr = static_cast<const uint8_t*>(x) + t * K;
+                const uint8_t* wr = static_cast<const uint8_t*>(W) + ((int64_t)e * N + n) * K;
+                for (int kb = 0; kb < KB; ++kb) {
+                    double part = 0.0;
+                    for (int c = kb * 128; c < kb * 128 + 128; ++c) part += (double)dec[xr[c]] * (double)dec[wr[c]];
+                    acc += (double)xs[t * KB + kb] * (double)Ws[((int64_t)e * NB + n / 128) * KB + kb] * part;
+                }
+            }
+            o[n] = static_cast<float>(acc);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- SwiGLU
 // silu(gate) * up on the gate_up output (LlamaFactory write-up, section 1):
 // gate = Y1[p, :I] (first half of W1's rows), up = Y1[p, I:].  Rows at or

@@ -21,7 +21,7 @@ __all__ = [
     "build", "use_openmp", "threads", "e4m3_encode", "e4m3_decode", "bf16_round", "route_topk",
     "mark_sentinels", "ep_local_ids", "sort_by_expert", "quant_act_fp8", "quant_weight_fp8", "permute",
     "grouped_gemm_bf16", "grouped_gemm_fp8", "swiglu", "combine", "moe_forward",
-    "grouped_gemm_dgrad_bf16", "grouped_gemm_wgrad_bf16",
+    "grouped_gemm_dgrad_bf16", "grouped_gemm_wgrad_bf16", "batched_matmul",
 ]
 
 
@@ -227,6 +227,24 @@ def grouped_gemm_fp8(qa, sa, qb, sb, offsets, rows=None):
     _L().orc_grouped_gemm_fp8(_p(qa), _p(sa), _p(qb), _p(sb), _p(off), E, C.c_int64(M_cap), N, K,
                               _p(rows), C.c_int64(0 if rows is None else rows.size), _p(Cm))
     return Cm
+
+
+def batched_matmul(x, ids, W, E: int, x_scales=None, W_scales=None):
+    """out [T*k, N] fp32: for slot f = t*k + j with expert e = ids[t, j] < E,
+    out[f] = W[e] x[t] (bf16 bits, or e4m3 bytes with their scales); sentinel
+    slots give zero rows."""
+    fp8 = W_scales is not None
+    x = np.ascontiguousarray(x, np.uint8 if fp8 else np.uint16)
+    W = np.ascontiguousarray(W, np.uint8 if fp8 else np.uint16)
+    ids = _c(ids, np.int32)
+    T, K = x.shape
+    k = ids.shape[1]
+    E2, N, K2 = W.shape
+    assert K == K2 and ids.shape[0] == T
+    out = np.empty((T * k, N), np.float32)
+    _L().orc_batched_matmul(int(fp8), _p(x), _p(_c(x_scales, np.float32)), _p(ids), C.c_int64(T), k, E, _p(W),
+                            _p(_c(W_scales, np.float32)), N, K, _p(out))
+    return out
 
 
 def swiglu(Y1, L: int):
