@@ -60,6 +60,8 @@ _SIGS = {
     "moe_grouped_gemm_dgrad": (_S, [_P, _P, _P, _I, _I, _I, _I, _P, _P, C.c_size_t, _P]),
     "moe_grouped_gemm_wgrad_workspace_size": (C.c_size_t, [_I, _I, _I, _I]),
     "moe_grouped_gemm_wgrad": (_S, [_P, _P, _P, _I, _I, _I, _I, _P, _P, C.c_size_t, _P]),
+    "moe_batched_matmul_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "moe_batched_matmul": (_S, [_I, _P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _P, _Z, _P]),
     "moe_swiglu": (_S, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_combine": (_S, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_forward_workspace_size": (_Z, [C.POINTER(ForwardArgs)]),
@@ -205,6 +207,15 @@ def moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K) -> int:
 def moe_grouped_gemm_wgrad(A, dC, offsets, E, M_cap, N, K, dB, ws, ws_bytes, stream=None):
     _check(lib().moe_grouped_gemm_wgrad(_p(A), _p(dC), _p(offsets), E, M_cap, N, K, _p(dB), _p(ws), ws_bytes,
                                         _stream(stream)), "moe_grouped_gemm_wgrad")
+
+
+def moe_batched_matmul_workspace_size(dtype, T, K, k, E, N) -> int:
+    return lib().moe_batched_matmul_workspace_size(dtype, T, K, k, E, N)
+
+
+def moe_batched_matmul(dtype, x, x_scales, T, K, topk_ids, k, W, W_scales, E, N, out, ws, ws_bytes, stream=None):
+    _check(lib().moe_batched_matmul(dtype, _p(x), _p(x_scales), T, K, _p(topk_ids), k, _p(W), _p(W_scales), E, N,
+                                    _p(out), _p(ws), ws_bytes, _stream(stream)), "moe_batched_matmul")
 
 
 def moe_swiglu(Y1, offsets, E, M_cap, I, h, stream=None):

@@ -333,6 +333,32 @@ moe_status_t moe_grouped_gemm_wgrad(const void* A, const void* dC, const int32_t
                                     moe_stream_t stream);
 
 /*
+ * moe_batched_matmul -- the batched expert backend ("Mixture of Experts in
+ * transformers", pluggable expert backends: batched_mm; batched_fp8_matmul
+ * in section 1 of the transformers MoE/FP8 write-up): every routed (token,
+ * expert) product on its own, without weighting or a sum over the picks:
+ *   out[t*k + j, n] = sum_c x[t, c] * W[e, n, c],   e = topk_ids[t, j] < E,
+ * with fp32 accumulation (FP8: the block-scaled sum of moe_grouped_gemm),
+ * stored bf16; a sentinel slot (id E) gets a zero row.  Computed by sorting
+ * the slots by expert and running one grouped GEMM (each expert's weights
+ * are read once per call), then gathering the product rows back into slot
+ * order; the results equal moe_permute + moe_grouped_gemm's rows bit for bit.
+ * x        bf16 [T, K], or e4m3 [T, K] with x_scales fp32 [T, K/128]
+ *          (row-major, as moe_act_quant_fp8 writes them)
+ * topk_ids int32 [T, k] (device; read only -- an id outside [0, E] is
+ *          recorded as MOE_DEVERR_ROUTE and its row is zero)
+ * W        bf16 [E, N, K], or e4m3 with W_scales fp32 [E, N/128, K/128]
+ * out      bf16 [T*k, N]
+ * ws       moe_batched_matmul_workspace_size(dtype, T, K, k, E, N) bytes
+ * Limits: 1 <= E <= 256, 1 <= k <= min(E, 32), T*k < 2^31; bf16: N, K
+ *   multiples of 8; FP8: N and K multiples of 128.
+ */
+size_t moe_batched_matmul_workspace_size(moe_dtype_t dtype, int T, int K, int k, int E, int N);
+moe_status_t moe_batched_matmul(moe_dtype_t dtype, const void* x, const float* x_scales, int T, int K,
+                                const int32_t* topk_ids, int k, const void* W, const float* W_scales, int E,
+                                int N, void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_swiglu -- standalone silu(gate) * up (LlamaFactory write-up, section
  * 1): h[p, n] = g / (1 + exp(-g)) * Y1[p, I + n] with g = Y1[p, n], for
  * p < offsets[E]; rows p >= offsets[E] of h are written as zeros.

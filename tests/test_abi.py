@@ -93,6 +93,10 @@ def test_workspace_sizes(moe):
     ("moe_grouped_gemm_gather", (0, 16, None, 4, 0, 16, 16, None, 16, 8, 64, 64, 64, 0, 16, None, None)),
     ("moe_grouped_gemm_gather", (0, 18, None, 4, 2, 16, 16, None, 16, 8, 64, 64, 64, 0, 16, None, None)),
     ("moe_grouped_gemm_gather", (1, 16, 16, 4, 2, 16, 16, 16, 16, 8, 64, 256, 100, 0, 16, None, None)),
+    # batched products: FP8 N not a multiple of 128, k > E, misaligned out
+    ("moe_batched_matmul", (1, 16, 16, 4, 256, 16, 2, 16, 16, 8, 200, 16, 16, 1 << 20, None)),
+    ("moe_batched_matmul", (0, 16, None, 4, 64, 16, 9, 16, None, 8, 64, 16, 16, 1 << 20, None)),
+    ("moe_batched_matmul", (0, 16, None, 4, 64, 16, 2, 16, None, 8, 64, 18, 16, 1 << 20, None)),
     ("moe_swiglu", (16, 16, 8, 64, 12, 16, None)),
     ("moe_combine", (16, 16, 16, 16, 4, 2, 12, 8, 16, None)),
     ("moe_combine", (16, 16, 16, 16, 4, 40, 16, 64, 16, None)),
@@ -130,6 +134,8 @@ def test_forward_gathers_only_whole_k_blocks(moe):
 @host_only
 def test_workspace_too_small_is_reported(moe):
     st = moe.lib().moe_route_sort(16, None, None, 16, 16, 64, 8, 2, 1, 16, 16, 16, 16, 4, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    st = moe.lib().moe_batched_matmul(0, 16, None, 4, 64, 16, 2, 16, None, 8, 64, 16, 16, 4, None)
     assert st == moe.MOE_ERR_WORKSPACE
 
 
