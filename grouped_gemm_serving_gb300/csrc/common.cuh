@@ -354,12 +354,31 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with the 128-byte swizzle: swizzle atoms of 64 16-bit elements along
+// M/N (128-byte rows) x the tile's K rows, the atoms `atom_bytes` apart;
+// within an atom, 8-row groups along K are 1024 bytes apart.  A K step of
+// the MMA advances the start address by 16 rows x 128 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t atom_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((atom_bytes >> 4) & 0x3FFFu) << 16;   // leading byte offset: next atom along M/N
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;                     // stride byte offset: next 8 rows of K
+    d |= static_cast<uint64_t>(1u) << 46;                             // version
+    d |= static_cast<uint64_t>(2u) << 61;                             // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for tcgen05.mma with fp32 accumulation, K-major A
 // and B: bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format
 // (kind::f16: 1 = bf16; kind::f8f6f4: 0 = e4m3), 17-22 N/8, 24-28 M/16.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, int M, int N) {
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// The same with A read MN-major (bit 15, "transpose A").
+__host__ __device__ constexpr uint32_t make_idesc_a_mn(uint32_t ab_format, int M, int N) {
+    return make_idesc(ab_format, M, N) | (1u << 15);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

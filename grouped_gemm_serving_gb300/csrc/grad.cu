@@ -3,9 +3,9 @@
 // transformers"; section 3 of "Hugging Face Transformers: MoE and FP8 kernel
 // optimisation": the gradients of sentinel rows must be written, as zeros).
 //
-//   dgrad  dA[p, c] = sum_n dC[p, n] B[e, n, c]: the forward grouped GEMM
-//          (moe_grouped_gemm) on B transposed to [E, K, N]; it writes zeros for
-//          the sentinel rows and never reads them.
+//   dgrad  dA[p, c] = sum_n dC[p, n] B[e, n, c]: the grouped GEMM kernel with
+//          B read in place as an MN-major operand (the c features contiguous);
+//          it writes zeros for the sentinel rows and never reads them.
 //   wgrad  dB[e, n, c] = sum over expert e's rows of dC[p, n] A[p, c]: dC and A
 //          are transposed so that each expert's rows run along the contraction
 //          dimension from a 64-aligned start, zero-padded to whole 64-element
@@ -59,16 +59,6 @@ __device__ __forceinline__ void transpose_tile(const uint16_t* __restrict__ src,
         }
     }
     __syncthreads();
-}
-
-// Wt[e, k, n] = W[e, n, k]; one 64 x 64 tile per CTA (N, K multiples of 8).
-__global__ void __launch_bounds__(256)
-transpose_weights_kernel(const uint16_t* __restrict__ W, int N, int K, uint16_t* __restrict__ Wt) {
-    __shared__ __align__(16) uint16_t tile[kTile][kPitch];
-    const int e = blockIdx.z, n0 = blockIdx.y * kTile, k0 = blockIdx.x * kTile;
-    const int64_t base = static_cast<int64_t>(e) * N * K;
-    transpose_tile(W + base, K, K, [&](int r) -> int64_t { return n0 + r < N ? n0 + r : -1; }, Wt + base, N, n0, N,
-                   k0, tile);
 }
 
 // Xt[c, q] for q in [0, P): the row of X that expert e's padded run puts at q,
@@ -148,27 +138,18 @@ int64_t padded_cols(int E, int M_cap) {
 }  // namespace
 
 extern "C" size_t moe_grouped_gemm_dgrad_workspace_size(int E, int N, int K) {
-    if (E < 1 || E > kMaxE || N < 8 || K < 8) return 0;
-    return static_cast<size_t>(E) * N * K * 2;
+    (void)E; (void)N; (void)K;
+    return 0;   // the weights are read in place
 }
 
 extern "C" moe_status_t moe_grouped_gemm_dgrad(const void* dC, const void* B, const int32_t* offsets, int E,
                                                int M_cap, int N, int K, void* dA, void* ws, size_t ws_bytes,
                                                moe_stream_t stream) {
+    (void)ws; (void)ws_bytes;
     MOE_CHECK_ARG(dC && B && offsets && dA && E >= 1 && E <= kMaxE && M_cap >= 1);
     MOE_CHECK_ARG(N >= 8 && N % 8 == 0 && K >= 8 && K % 8 == 0);
     MOE_CHECK_ARG(moe::aligned16(dC) && moe::aligned16(B) && moe::aligned16(dA));
-    const size_t need = moe_grouped_gemm_dgrad_workspace_size(E, N, K);
-    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
-    MOE_CHECK_ARG(moe::aligned16(ws));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint16_t* Bt = static_cast<uint16_t*>(ws);
-    const dim3 grid((K + kTile - 1) / kTile, (N + kTile - 1) / kTile, E);
-    transpose_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(B), N, K, Bt);
-    MOE_CHECK_LAUNCH();
-    // dA = dC Bt[e]^T with Bt [E, K, N]: the forward GEMM, N and K exchanged
-    return moe_grouped_gemm(MOE_BF16, dC, nullptr, Bt, nullptr, offsets, E, M_cap, K, N, MOE_EPI_STORE, dA,
-                            nullptr, stream);
+    return moe::dgrad_gemm(dC, B, offsets, E, M_cap, N, K, dA, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t moe_grouped_gemm_wgrad_workspace_size(int E, int M_cap, int N, int K) {

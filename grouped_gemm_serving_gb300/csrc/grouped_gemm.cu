@@ -131,6 +131,10 @@ struct Params {
     // start, zero-padded; expert e's tile rows are all wg_rows rows and its K
     // range its own k-blocks; the output is [E, wg_rows, N].
     int wg, wg_rows;
+    // swapped store tiles only: the weights are MN-major, B [E, K, N] with
+    // the N output features contiguous (the data gradient reads the forward
+    // weights [E, N_fwd, K_fwd] in place this way)
+    int mn_a;
 };
 
 // Shared memory after the stage ring: barriers and the tile list (every
@@ -370,7 +374,12 @@ __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX3
             const int kc = kb * 64;
             if (moe::elect_one()) {
                 if (rank == 0) moe::mbar_arrive_expect_tx(bar(S.full[stage]), 2 * (kStageA + xbytes));
-                if (EPI == EPI_STORE)
+                if (EPI == EPI_STORE && p.mn_a) {
+                    // two 64-feature x 64-row swizzle atoms, 8 KB apart
+                    const int f0 = ti.col0 + static_cast<int>(rank) * 128;
+                    moe::tma_load_3d_pair(sa, tmW, fb, f0, kc, ti.e);
+                    moe::tma_load_3d_pair(sa + 8192, tmW, fb, f0 + 64, kc, ti.e);
+                } else if (EPI == EPI_STORE)
                     moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
                 else
                     moe::tma_load_4d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 64, 0, ti.e);
@@ -509,7 +518,10 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued = false;
     for (int t = tile_first<SWAP>(); ok && t < total; t += tile_step<SWAP>()) {
-        if (SWAP) idesc = moe::make_idesc(1u, 2 * BM, swap_n(decode_tile<true>(t, S, p)));
+        if (SWAP) {
+            const int n = swap_n(decode_tile<true>(t, S, p));
+            idesc = EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n) : moe::make_idesc(1u, 2 * BM, n);
+        }
         if (!FP8) {
             // with a pair, the peer's epilogue arrives here from the other CTA
             const bool got = SWAP ? moe::mbar_wait_cluster(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs)
@@ -530,7 +542,11 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             moe::tc_fence_after();
             const uint32_t sa = moe::smem_u32(stages + stage * Geo<SWAP, EPI>::kStageBytes);
-            const uint64_t adesc = moe::smem_desc_sw128(sa);
+            // MN-major weights (swapped store tiles of the data gradient): a K
+            // step of 16 rows is 2 KB further on; K-major: 32 bytes
+            const bool amn = SWAP && EPI == EPI_STORE && p.mn_a;
+            const uint64_t adesc = amn ? moe::smem_desc_sw128_mn(sa, 8192) : moe::smem_desc_sw128(sa);
+            const uint64_t astep = amn ? 2048 >> 4 : 2;
             const uint64_t bdesc = moe::smem_desc_sw128(sa + kStageA);
             const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
             // the same (lowest) lane is elected every time, so its commits
@@ -541,7 +557,7 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
                     if (FP8)
                         moe::mma_fp8(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0);
                     else if (SWAP)
-                        moe::mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                        moe::mma_bf16_pair(d, adesc + astep * k, bdesc + 2 * k, idesc, (kb | k) != 0);
                     else
                         moe::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
                 if (SWAP) moe::tc_commit_pair(bar(S.empty[stage]), 0x3);   // frees the stage in both CTAs
@@ -1074,10 +1090,12 @@ moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtens
 
 // Shared by both entry points.  With gx set, A is gathered from token order
 // (gx [T, K], sorted_rows [T*topk]) and the A tensor map is never used.
+// With weights_mn (bf16 store only) B is [E, K, N], read MN-major.
 moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales, const void* gx,
                               const int32_t* sorted_rows, int T, int topk, const void* B,
                               const float* B_scales, const int32_t* offsets, int E, int M_cap, int N, int K,
-                              moe_epilogue_t epilogue, void* C, float* C_scales, moe_stream_t stream) {
+                              moe_epilogue_t epilogue, void* C, float* C_scales, moe_stream_t stream,
+                              bool weights_mn = false) {
     MOE_CHECK_ARG(A && B && offsets && C && E >= 1 && E <= kMaxE && M_cap >= 1 && N >= 8 && K >= 8);
     MOE_CHECK_ARG(moe::aligned16(A) && moe::aligned16(B) && moe::aligned16(C));
     const bool fp8 = dtype == MOE_FP8_E4M3_B128;
@@ -1126,7 +1144,14 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
         if (!encode(&tmA128, fp8, A, 2, dims, strides, box128)) return MOE_ERR_CUDA;
         if (!encode(&tmA32, fp8, A, 2, dims, strides, box32)) return MOE_ERR_CUDA;
     }
-    if (!swiglu) {
+    if (weights_mn) {
+        if (fp8 || swiglu || gx) return MOE_ERR_UNSUPPORTED;
+        // [E, K, N] with N contiguous: 64-feature x 64-row boxes (one swizzle atom)
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(E)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(K) * N * 2};
+        const cuuint32_t box[3] = {64, 64, 1};
+        if (!encode(&tmB, false, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
+    } else if (!swiglu) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(N) * K * esz};
         const cuuint32_t box[3] = {bk, swap ? 128u : BN, 1};   // swapped: 128 weight rows per CTA
@@ -1164,6 +1189,7 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     p.topk = gx ? topk : 1;
     p.wg = 0;
     p.wg_rows = 0;
+    p.mn_a = weights_mn ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fp8) {
         if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
@@ -1179,6 +1205,15 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
 }
 
 }  // namespace
+
+moe_status_t moe::dgrad_gemm(const void* dC, const void* B, const int32_t* offsets, int E, int M_cap, int N, int K,
+                             void* dA, cudaStream_t s) {
+    // dA [M_cap, K] = dC [M_cap, N] x B[e] [N, K]: a store GEMM with K output
+    // features over an N-long contraction, the weights B [E, N, K] read
+    // MN-major in place
+    return run_grouped_gemm(MOE_BF16, dC, nullptr, nullptr, nullptr, 0, 0, B, nullptr, offsets, E, M_cap, K, N,
+                            MOE_EPI_STORE, dA, nullptr, reinterpret_cast<moe_stream_t>(s), true);
+}
 
 moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, const int32_t* offsets, int E,
                              int M_cap, int N, int K, void* dB, cudaStream_t s) {

@@ -5,6 +5,13 @@
 
 namespace moe {
 
+// Launches the bf16 grouped GEMM for the data gradient (grouped_gemm.cu):
+//   dA[p, c] = sum_n dC[p, n] * B[e, n, c]   (rows p of expert e)
+// with B [E, N, K] read in place (MN-major); rows p >= offsets[E] of dA are
+// zeros.  dC bf16 [M_cap, N], dA bf16 [M_cap, K].
+moe_status_t dgrad_gemm(const void* dC, const void* B, const int32_t* offsets, int E, int M_cap, int N, int K,
+                        void* dA, cudaStream_t stream);
+
 // Launches the grouped GEMM in its weight-gradient mode (grouped_gemm.cu):
 //   dB[e, n, c] = sum_j At_g[n, P_e + j] * Bt_g[c, P_e + j]
 // over expert e's zero-padded run [P_e, P_e + 64 * ceil(cnt_e / 64)) of the

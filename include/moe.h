@@ -310,9 +310,10 @@ moe_status_t moe_grouped_gemm_gather(moe_dtype_t dtype, const void* x, const flo
  *
  * moe_grouped_gemm_dgrad:  dA[p, c] = sum_n dC[p, n] * B[e, n, c] for p <
  *   offsets[E]; rows p >= offsets[E] of dA are zeros (dC's are never read).
- *   dC bf16 [M_cap, N]; B bf16 [E, N, K]; dA bf16 [M_cap, K].
- *   Workspace: moe_grouped_gemm_dgrad_workspace_size(E, N, K) bytes (B
- *   transposed).
+ *   dC bf16 [M_cap, N]; B bf16 [E, N, K]; dA bf16 [M_cap, K].  B is read in
+ *   place (its K features contiguous, an MN-major operand of the tensor
+ *   cores): moe_grouped_gemm_dgrad_workspace_size returns 0 and ws may be
+ *   NULL.
  * moe_grouped_gemm_wgrad:  dB[e, n, c] = sum over p in [offsets[e],
  *   offsets[e+1]) of dC[p, n] * A[p, c]; an expert without rows gets zeros;
  *   rows p >= offsets[E] of A and dC are never read.

@@ -141,3 +141,15 @@ def test_gradients_are_bit_reproducible(moe):
         assert moe.moe_get_device_error() == 0
         outs.append((host_bf16_bits(dA), host_bf16_bits(dB)))
     assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_dgrad_needs_no_workspace(moe):
+    """The data gradient reads the weights in place (MN-major): no workspace."""
+    E, M_cap, live, N, K = 5, 700, 650, 320, 192
+    off, live, A, B, dC = _operands(E, M_cap, live, N, K, seed=17, counts=None)
+    assert moe.moe_grouped_gemm_dgrad_workspace_size(E, N, K) == 0
+    dA = torch.full((M_cap, K), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm_dgrad(dev_bf16(dC), dev_bf16(B), dev(off), E, M_cap, N, K, dA, None, 0)
+    assert moe.moe_get_device_error() == 0
+    assert_close_bf16(host_f32_from_bf16(dA)[:live], oracle.grouped_gemm_dgrad_bf16(dC, B, off)[:live])
+    assert np.all(host_bf16_bits(dA)[live:] == 0)
