@@ -319,6 +319,14 @@ def layer_summary(wl, step, step_ms, separate, pk):
                       "hbm_gbs": by / t / 1e9, "hbm_frac": by / t / 1e9 / hbm,
                       "roofline_frac": max(fl / (tpeak * 1e12), by / (hbm * 1e9)) / t,
                       "algorithmic_flop": fl, "algorithmic_bytes": by}
+    # DRAM traffic per launch from an ncu capture of this workload, where
+    # profiles/ holds one (null otherwise)
+    tp = os.path.join(ROOT, "profiles", f"traffic_{wl.name}.json")
+    if os.path.exists(tp) and separate:
+        with open(tp) as f:
+            tr = json.load(f)
+        gemm["gate_up"]["traffic"] = tr.get("gemm_gate_up_swiglu_bytes")
+        gemm["down"]["traffic"] = tr.get("gemm_down_bytes")
     data = {}
     for name, key in (("route_sort", "route_bytes"), ("act_quant", "act_quant_bytes"),
                       ("permute", "permute_bytes"), ("combine", "combine_bytes")):
