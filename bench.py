@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--gather", action="store_true",
                     help="gather the gate_up GEMM's rows from token order inside the GEMM "
                          "(moe_forward's MOE_FWD_GATHER) instead of a separate permute")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="fold the weighted combine into the down GEMM (moe_forward's "
+                         "MOE_FWD_FUSED_COMBINE; bf16 workloads)")
     ap.add_argument("--ncu", action="store_true",
                     help="profiler mode: W warm-up steps then K steps, nothing else (no clock "
                          "pre-roll, end-to-end pass or CPU baseline), so launches can be counted")
@@ -191,9 +194,10 @@ class Step:
     """The hot path as the chain of C-ABI calls moe_forward enqueues, with
     CUDA events between kernels on the launching stream."""
 
-    def __init__(self, wl, L, torch, moe, separate_scatter=True):
+    def __init__(self, wl, L, torch, moe, separate_scatter=True, fused_combine=False):
         self.wl, self.L, self.torch, self.moe = wl, L, torch, moe
         self.scatter = separate_scatter
+        self.fused = fused_combine and wl.dtype != "fp8"
         T, E, k, H, I = wl.T, wl.E, wl.k, wl.H, wl.I
         R = T * k
         self.fp8 = wl.dtype == "fp8"
@@ -215,7 +219,11 @@ class Step:
         self.y2 = z(R, H, dt=torch.bfloat16)
         self.out = z(T, H, dt=torch.bfloat16)
         self.names = (["route_sort"] + (["act_quant"] if self.fp8 else []) +
-                      (["permute"] if self.scatter else []) + ["gemm_gate_up_swiglu", "gemm_down", "combine"])
+                      (["permute"] if self.scatter else []) + ["gemm_gate_up_swiglu", "gemm_down"] +
+                      ([] if self.fused else ["combine"]))
+        if self.fused:
+            self.cws_bytes = moe.moe_grouped_gemm_combine_workspace_size(T, H)
+            self.cws = z(self.cws_bytes)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(self.names) + 1)]
         self.times = {n: [] for n in self.names}
 
@@ -258,11 +266,16 @@ class Step:
                 moe.moe_grouped_gemm_gather(moe.MOE_BF16, L["x"], None, T, k, self.sr, L["w1"], None, self.off,
                                             E, R, 2 * I, H, moe.MOE_EPI_SWIGLU, self.h, None)
             mark()
-            moe.moe_grouped_gemm(moe.MOE_BF16, self.h, None, L["w2"], None, self.off, E, R, H, I,
-                                 moe.MOE_EPI_STORE, self.y2, None)
+            if self.fused:
+                moe.moe_grouped_gemm_combine(self.h, L["w2"], self.off, E, R, H, I, self.ids, self.w, self.sr, self.rp,
+                                             T, k, self.y2, self.out, self.cws, self.cws_bytes)
+            else:
+                moe.moe_grouped_gemm(moe.MOE_BF16, self.h, None, L["w2"], None, self.off, E, R, H, I,
+                                     moe.MOE_EPI_STORE, self.y2, None)
         mark()
-        moe.moe_combine(self.y2, self.ids, self.w, self.rp, T, k, H, E, self.out)
-        mark()
+        if not self.fused:
+            moe.moe_combine(self.y2, self.ids, self.w, self.rp, T, k, H, E, self.out)
+            mark()
 
     def collect(self):
         for i, n in enumerate(self.names):
@@ -813,7 +826,7 @@ def main():
 
     L = make_layer(wl, torch, moe, synth)
     separate = not (args.gather and (wl.H * (1 if wl.dtype == "fp8" else 2)) % 128 == 0)
-    step = Step(wl, L, torch, moe, separate_scatter=separate)
+    step = Step(wl, L, torch, moe, separate_scatter=separate, fused_combine=args.fused_combine)
     if args.ncu:
         for _ in range(args.warmup + args.steps):
             step.run()
@@ -848,7 +861,8 @@ def main():
                           k=wl.k, H=wl.H, I=wl.I, x=x_pin, W1=L["w1"], W2=L["w2"], W1_scales=L.get("w1_s"),
                           W2_scales=L.get("w2_s"), out=out_pin, logits=lg_pin, expert_bias=L["bias"],
                           sentinel_mask=L["mask"],
-                          renormalize=wl.renormalize, host_io=True, gather=not separate)
+                          renormalize=wl.renormalize, host_io=True, gather=not separate,
+                          fused_combine=step.fused)
     nws = moe.moe_forward_workspace_size(fa)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -882,7 +896,7 @@ def main():
                                W1=L["w1"], W2=L["w2"], W1_scales=L.get("w1_s"), W2_scales=L.get("w2_s"),
                                out=d_out[i], logits=d_lg[i], expert_bias=L["bias"], sentinel_mask=L["mask"],
                                renormalize=wl.renormalize,
-                               gather=not separate) for i in range(2)]
+                               gather=not separate, fused_combine=step.fused) for i in range(2)]
     s_comp, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in_ready", "in_free", "out_ready", "out_free")}
     # each staging slot's moe_forward call captured once, like the step above
@@ -994,6 +1008,7 @@ def main():
                    "bias": wl.bias, "live_rows": live, "experts_with_rows": experts_live,
                    "parallelism": f"replicas x{world} (no collective)",
                    "scatter": "separate kernel" if separate else "gathered inside the gate_up GEMM",
+                   "combine": "fused into the down GEMM" if step.fused else "separate kernel",
                    "l2": "flushed between timed steps (256 MiB write, then read back; untimed)",
                    "launch": "eager C-ABI calls" if args.no_graph else "CUDA graph of the step's C-ABI calls"},
         "roofline": roofline,
@@ -1006,7 +1021,7 @@ def main():
                  "detail": summ["gemm"]},
         "kernels_ms": summ["kernels_ms"],
         "hbm": {"permute_gbs": summ["data_movement"].get("permute", {}).get("gbs"),
-                "combine_gbs": summ["data_movement"]["combine"]["gbs"],
+                "combine_gbs": summ["data_movement"].get("combine", {}).get("gbs"),
                 "peak_gbs": pk["hbm_gbs"], "detail": summ["data_movement"]},
         "e2e": {"value": job_tokens_per_s(wl.T, world, e2e_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,

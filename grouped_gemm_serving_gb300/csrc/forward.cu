@@ -32,6 +32,7 @@ struct Layout {
     size_t h, hs;           // gate_up output after SwiGLU (+ FP8 scales)
     size_t y2;              // down output, bf16
     size_t x_dev, logits_dev, out_dev;  // host-I/O staging
+    size_t counters;        // fused combine (bf16)
     size_t total;
 };
 
@@ -84,6 +85,7 @@ Layout layout(const moe_forward_args* a) {
         l.h = c.take(R * I * 2);
     }
     l.y2 = c.take(R * H * 2);
+    if ((a->flags & MOE_FWD_FUSED_COMBINE) && !fp8) l.counters = c.take(moe_grouped_gemm_combine_workspace_size(a->T, a->H));
     if (a->flags & MOE_FWD_HOST_IO) {
         l.x_dev = c.take(T * H * 2);
         l.logits_dev = a->logits ? c.take(T * E * 4) : 0;
@@ -226,8 +228,14 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
             MOE_TRY(moe_grouped_gemm_gather(MOE_BF16, x, nullptr, T, k, sorted_rows, a->W1, nullptr, offsets, E,
                                             R, 2 * I, H, MOE_EPI_SWIGLU, h, nullptr, stream));
         }
-        MOE_TRY(moe_grouped_gemm(MOE_BF16, h, nullptr, a->W2, nullptr, offsets, E, R, H, I,
-                                 MOE_EPI_STORE, y2, nullptr, stream));
+        if (a->flags & MOE_FWD_FUSED_COMBINE) {
+            MOE_TRY(moe_grouped_gemm_combine(h, a->W2, offsets, E, R, H, I, ids, w, sorted_rows, row_pos, T, k, y2,
+                                             out, base + l.counters, moe_grouped_gemm_combine_workspace_size(T, H),
+                                             stream));
+        } else {
+            MOE_TRY(moe_grouped_gemm(MOE_BF16, h, nullptr, a->W2, nullptr, offsets, E, R, H, I,
+                                     MOE_EPI_STORE, y2, nullptr, stream));
+        }
     } else {
         uint8_t* xq = base + l.xq;
         float* xs = reinterpret_cast<float*>(base + l.xs);
@@ -247,7 +255,7 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
         MOE_TRY(moe_grouped_gemm(MOE_FP8_E4M3_B128, h, hs, a->W2, a->W2_scales, offsets, E, R, H, I,
                                  MOE_EPI_STORE, y2, nullptr, stream));
     }
-    MOE_TRY(moe_combine(y2, ids, w, row_pos, T, k, H, E, out, stream));
+    if (fp8 || !(a->flags & MOE_FWD_FUSED_COMBINE)) MOE_TRY(moe_combine(y2, ids, w, row_pos, T, k, H, E, out, stream));
     if (copy_out)
         MOE_CHECK_CUDA(cudaMemcpyAsync(a->out, out, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost, s));
     return MOE_OK;

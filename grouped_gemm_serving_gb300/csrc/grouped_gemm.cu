@@ -135,6 +135,17 @@ struct Params {
     // the N output features contiguous (the data gradient reads the forward
     // weights [E, N_fwd, K_fwd] in place this way)
     int mn_a;
+    // swapped store tiles only: the weighted combine fused into the epilogue
+    // (moe_grouped_gemm_combine).  sorted_rows and topk (above) map a row to
+    // its token; counters [T, nfb] count the stored slots of each (token,
+    // 128-feature block) and start at zero.
+    int fc;
+    const int32_t* ids;
+    const float* wts;
+    const int32_t* row_pos;
+    int* counters;
+    int nfb;
+    void* cout;   // out bf16 [T, out_cols]
 };
 
 // Shared memory after the stage ring: barriers and the tile list (every
@@ -144,6 +155,7 @@ struct alignas(16) Shared {
     uint64_t acc_full[2], acc_empty[2];
     uint64_t xbar[2];  // amax exchange of the quantising epilogue
     uint64_t mma_done;
+    uint64_t cbar;     // fused combine: every epilogue thread has stored its rows of the tile
     // swapped SwiGLU: per epilogue warp pair, channel 0 carries gate values to
     // the up warp and channel 1 up values to the gate warp (half a chunk each)
     uint64_t xfull[4][2], xempty[4][2];
@@ -596,6 +608,127 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
     }
 }
 
+// Fused weighted combine, one 16-byte chunk (8 features) of token t's
+// 128-feature block at f0: out[t, f] = sum over live slots j, in slot order,
+// of w[t, j] * Y2[row_pos[t*k + j], f], accumulated in fp32 with fmaf exactly
+// as moe_combine does, rounded to bf16.  The rows come through L2 (other
+// CTAs stored most of them).
+__device__ __forceinline__ void combine_chunk(const Params& p, int t, int f0, int c) {
+    const int f = f0 + 8 * c;
+    if (f >= p.out_cols) return;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    const __nv_bfloat16* Y2 = static_cast<const __nv_bfloat16*>(p.out);
+    // up to eight slots at a time: their rows are all requested before the
+    // first is summed, so the loads are in flight together
+    constexpr int G = 8;
+    for (int j0 = 0; j0 < p.topk; j0 += G) {
+        uint4 v[G];
+        float wj[G];
+        bool use[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int j = j0 + g;
+            use[g] = false;
+            wj[g] = 0.0f;
+            v[g] = make_uint4(0, 0, 0, 0);
+            if (j < p.topk) {
+                const int64_t slot = static_cast<int64_t>(t) * p.topk + j;
+                if (p.ids[slot] != p.E) {
+                    const int pos = p.row_pos[slot];
+                    if (pos < 0 || pos >= p.M_cap) {
+                        moe::raise_device_error(p.err, MOE_DEVERR_ROUTE);
+                    } else {
+                        use[g] = true;
+                        wj[g] = p.wts[slot];
+                        v[g] = __ldcg(reinterpret_cast<const uint4*>(Y2 + static_cast<int64_t>(pos) * p.out_cols + f));
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (!use[g]) continue;
+            const uint32_t v4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(wj[g], moe::bf16_lo(v4[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wj[g], moe::bf16_hi(v4[i]), acc[2 * i + 1]);
+            }
+        }
+    }
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.cout) + static_cast<int64_t>(t) * p.out_cols + f;
+    *reinterpret_cast<uint4*>(out) = make_uint4(moe::pack_bf16x2(acc[0], acc[1]), moe::pack_bf16x2(acc[2], acc[3]),
+                                                moe::pack_bf16x2(acc[4], acc[5]), moe::pack_bf16x2(acc[6], acc[7]));
+}
+
+// After a swapped store tile: every epilogue thread of the CTA has stored
+// its rows of the tile (and fenced them; a bounded mbarrier wait, not a
+// hardware barrier, so that a CTA winding down after a timeout cannot hang
+// it); then each token of the tile bumps
+// the counter of its (token, 128-feature block).  The thread that brings it
+// to the token's number of live slots holds the last of them: its warp sums
+// that token's block (two tokens at a time, 16 lanes each) and resets the
+// counter.  Every (token, block) is summed once, in slot order, whichever CTA
+// stores last, so the result is the same bits as moe_combine's.
+__device__ __forceinline__ bool fused_combine_tile(Shared& S, const Params& p, const Tile& ti, uint32_t rank,
+                                                   uint32_t& cph) {
+    __threadfence();
+    moe::mbar_arrive(bar(S.cbar));
+    if (!moe::mbar_wait(bar(S.cbar), cph, &S.abort_flag, kWaitNs)) return false;
+    cph ^= 1u;
+    const int f0 = ti.col0 + static_cast<int>(rank) * 128;
+    if (f0 >= p.out_cols) return true;
+    const int fb = f0 / 128;
+    const int et = threadIdx.x - 128, lane = threadIdx.x & 31;
+    int t = 0;
+    bool last = false;
+    if (et < ti.rows) {
+        const int slot = p.sorted_rows[ti.row0 + et];
+        t = slot / p.topk;
+        if (t >= 0 && t < p.T) {
+            int live = 0;
+            for (int j = 0; j < p.topk; ++j) live += p.ids[static_cast<int64_t>(t) * p.topk + j] != p.E;
+            int* c = p.counters + static_cast<int64_t>(t) * p.nfb + fb;
+            last = atomicAdd(c, 1) == live - 1;
+            if (last) *c = 0;   // no other slot of this token touches it in this call
+        } else {
+            moe::raise_device_error(p.err, MOE_DEVERR_ROUTE);
+        }
+    }
+    unsigned mask = __ballot_sync(0xffffffffu, last);
+    if (mask) __threadfence();   // the other contributors' rows are visible from here on
+    while (mask) {
+        const int a = __ffs(mask) - 1;
+        mask &= mask - 1;
+        int b = -1;
+        if (mask) {
+            b = __ffs(mask) - 1;
+            mask &= mask - 1;
+        }
+        const int ta = __shfl_sync(0xffffffffu, t, a);
+        const int tb = __shfl_sync(0xffffffffu, t, b < 0 ? a : b);
+        if (lane < 16) combine_chunk(p, ta, f0, lane);
+        else if (b >= 0) combine_chunk(p, tb, f0, lane - 16);
+    }
+    return true;
+}
+
+// Tokens whose slots are all sentinels get no contribution: their output
+// rows are zeros (spread over every epilogue thread of the grid).
+__device__ void fused_combine_empty_tokens(const Params& p) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kEpiThreads + (threadIdx.x - 128);
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * kEpiThreads;
+    for (int64_t t = tid; t < p.T; t += nthr) {
+        bool any = false;
+        for (int j = 0; j < p.topk; ++j) any |= p.ids[t * p.topk + j] != p.E;
+        if (any) continue;
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.cout) + t * p.out_cols);
+        for (int v = 0; v < p.out_cols / 8; ++v) o[v] = make_uint4(0, 0, 0, 0);
+    }
+}
+
 template <bool FP8, int EPI, bool SWAP>
 __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -607,6 +740,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
     uint32_t acc_phase = 0, xphase = 0;
     const int xp = (q & 1) + 2 * hsel;   // swapped SwiGLU: warp pair (gate q, up q + 2) of this column half
     uint32_t xph = 0;
+    uint32_t cph = 0;                    // fused combine barrier phase
     const int KB = p.k_blocks;
 
     // the pair's MMA waits for both CTAs' epilogues on the leader's barrier
@@ -679,6 +813,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             else moe::mbar_arrive(bar(S.acc_empty[acc]));
             acc ^= 1;
             if (!acc) acc_phase ^= 1u;
+            if (EPI == EPI_STORE && p.fc && !fused_combine_tile(S, p, ti, rank, cph)) { fail(S, p); return; }
         } else if (!FP8) {
             if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
             moe::tc_fence_after();
@@ -901,6 +1036,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             moe::mbar_init(bar(S.xbar[a]), kEpiThreads);
         }
         moe::mbar_init(bar(S.mma_done), 1);
+        moe::mbar_init(bar(S.cbar), kEpiThreads);
         for (int i = 0; i < 4; ++i)
             for (int c = 0; c < 2; ++c) {
                 moe::mbar_init(bar(S.xfull[i][c]), 32);
@@ -999,6 +1135,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (FP8) moe::reg_alloc<kRegsHigh>();
         epilogue<FP8, EPI, SWAP>(S, p, total, tmem, rank);
         if (!p.wg) zero_sentinel_rows<EPI>(p);
+        if (SWAP && EPI == EPI_STORE && p.fc) fused_combine_empty_tokens(p);
     } else {
         if (FP8) moe::reg_dealloc<kRegsLow>();
         if (!SWAP && p.gx && (warp == 0 || warp - 1 < kGatherWarps) && warp != 1) {
@@ -1090,12 +1227,24 @@ moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtens
 
 // Shared by both entry points.  With gx set, A is gathered from token order
 // (gx [T, K], sorted_rows [T*topk]) and the A tensor map is never used.
-// With weights_mn (bf16 store only) B is [E, K, N], read MN-major.
+// The fused weighted combine of moe_grouped_gemm_combine.
+struct FusedCombine {
+    const int32_t* ids;
+    const float* w;
+    const int32_t* sorted_rows;
+    const int32_t* row_pos;
+    int T, k;
+    int* counters;
+    void* out;
+};
+
+// With weights_mn (bf16 store only) B is [E, K, N], read MN-major.  With fc
+// (bf16 store only) the weighted combine is fused into the epilogue.
 moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales, const void* gx,
                               const int32_t* sorted_rows, int T, int topk, const void* B,
                               const float* B_scales, const int32_t* offsets, int E, int M_cap, int N, int K,
                               moe_epilogue_t epilogue, void* C, float* C_scales, moe_stream_t stream,
-                              bool weights_mn = false) {
+                              bool weights_mn = false, const FusedCombine* fc = nullptr) {
     MOE_CHECK_ARG(A && B && offsets && C && E >= 1 && E <= kMaxE && M_cap >= 1 && N >= 8 && K >= 8);
     MOE_CHECK_ARG(moe::aligned16(A) && moe::aligned16(B) && moe::aligned16(C));
     const bool fp8 = dtype == MOE_FP8_E4M3_B128;
@@ -1190,6 +1339,20 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     p.wg = 0;
     p.wg_rows = 0;
     p.mn_a = weights_mn ? 1 : 0;
+    p.fc = 0;
+    if (fc) {
+        if (fp8 || swiglu || gx || weights_mn) return MOE_ERR_UNSUPPORTED;
+        p.fc = 1;
+        p.ids = fc->ids;
+        p.wts = fc->w;
+        p.sorted_rows = fc->sorted_rows;
+        p.row_pos = fc->row_pos;
+        p.T = fc->T;
+        p.topk = fc->k;
+        p.counters = fc->counters;
+        p.nfb = (N + 127) / 128;
+        p.cout = fc->out;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fp8) {
         if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
@@ -1260,6 +1423,30 @@ extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const
                                          void* C, float* C_scales, moe_stream_t stream) {
     return run_grouped_gemm(dtype, A, A_scales, nullptr, nullptr, 0, 0, B, B_scales, offsets, E, M_cap, N, K,
                             epilogue, C, C_scales, stream);
+}
+
+extern "C" size_t moe_grouped_gemm_combine_workspace_size(int T, int H) {
+    if (T < 1 || H < 8) return 0;
+    const size_t bytes = static_cast<size_t>(T) * ((H + 127) / 128) * sizeof(int);
+    return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+extern "C" moe_status_t moe_grouped_gemm_combine(const void* h, const void* W2, const int32_t* offsets, int E,
+                                                 int M_cap, int H, int I, const int32_t* topk_ids,
+                                                 const float* topk_w, const int32_t* sorted_rows,
+                                                 const int32_t* row_pos, int T, int k, void* Y2, void* out,
+                                                 void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_CHECK_ARG(topk_ids && topk_w && sorted_rows && row_pos && out && T >= 1 && k >= 1 && k <= 32);
+    MOE_CHECK_ARG(static_cast<int64_t>(T) * k <= M_cap && H % 8 == 0);
+    MOE_CHECK_ARG(moe::aligned16(out) && moe::aligned16(topk_ids) && moe::aligned16(topk_w));
+    const size_t need = moe_grouped_gemm_combine_workspace_size(T, H);
+    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    MOE_CHECK_ARG(moe::aligned16(ws));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_CHECK_CUDA(cudaMemsetAsync(ws, 0, need, s));   // the per-(token, block) counters
+    const FusedCombine fc{topk_ids, topk_w, sorted_rows, row_pos, T, k, static_cast<int*>(ws), out};
+    return run_grouped_gemm(MOE_BF16, h, nullptr, nullptr, nullptr, 0, 0, W2, nullptr, offsets, E, M_cap, H, I,
+                            MOE_EPI_STORE, Y2, nullptr, stream, false, &fc);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_gather(moe_dtype_t dtype, const void* x, const float* x_scales, int T,

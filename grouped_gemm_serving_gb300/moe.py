@@ -23,6 +23,7 @@ MOE_EPI_STORE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_QUANT_FP8 = 0, 1, 2
 MOE_DEVERR_NONE, MOE_DEVERR_OFFSETS, MOE_DEVERR_TIMEOUT, MOE_DEVERR_ROUTE = 0, 1, 2, 3
 MOE_FWD_HOST_IO = 1
 MOE_FWD_GATHER = 2
+MOE_FWD_FUSED_COMBINE = 4
 
 
 class MoeError(RuntimeError):
@@ -62,6 +63,8 @@ _SIGS = {
     "moe_grouped_gemm_wgrad": (_S, [_P, _P, _P, _I, _I, _I, _I, _P, _P, C.c_size_t, _P]),
     "moe_batched_matmul_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_batched_matmul": (_S, [_I, _P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _P, _Z, _P]),
+    "moe_grouped_gemm_combine_workspace_size": (_Z, [_I, _I]),
+    "moe_grouped_gemm_combine": (_S, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_swiglu": (_S, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_combine": (_S, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_forward_workspace_size": (_Z, [C.POINTER(ForwardArgs)]),
@@ -218,6 +221,17 @@ def moe_batched_matmul(dtype, x, x_scales, T, K, topk_ids, k, W, W_scales, E, N,
                                     _p(out), _p(ws), ws_bytes, _stream(stream)), "moe_batched_matmul")
 
 
+def moe_grouped_gemm_combine_workspace_size(T, H) -> int:
+    return lib().moe_grouped_gemm_combine_workspace_size(T, H)
+
+
+def moe_grouped_gemm_combine(h, W2, offsets, E, M_cap, H, I, topk_ids, topk_w, sorted_rows, row_pos, T, k, Y2, out,
+                             ws, ws_bytes, stream=None):
+    _check(lib().moe_grouped_gemm_combine(_p(h), _p(W2), _p(offsets), E, M_cap, H, I, _p(topk_ids), _p(topk_w),
+                                          _p(sorted_rows), _p(row_pos), T, k, _p(Y2), _p(out), _p(ws), ws_bytes,
+                                          _stream(stream)), "moe_grouped_gemm_combine")
+
+
 def moe_swiglu(Y1, offsets, E, M_cap, I, h, stream=None):
     _check(lib().moe_swiglu(_p(Y1), _p(offsets), E, M_cap, I, _p(h), _stream(stream)), "moe_swiglu")
 
@@ -260,7 +274,7 @@ def route_sort_t(E: int, k: int, *, logits=None, expert_bias=None, sentinel_mask
 
 def forward_args(*, dtype, T, E, k, H, I, x, W1, W2, out, logits=None, expert_bias=None,
                  sentinel_mask=None, topk_ids=None, topk_w=None, W1_scales=None, W2_scales=None,
-                 renormalize=True, host_io=False, gather=False) -> ForwardArgs:
+                 renormalize=True, host_io=False, gather=False, fused_combine=False) -> ForwardArgs:
     """Fill a ForwardArgs from tensors (or raw addresses); ``gather`` sets
     MOE_FWD_GATHER.  The returned struct keeps the given tensors alive for as
     long as it lives."""
@@ -269,7 +283,8 @@ def forward_args(*, dtype, T, E, k, H, I, x, W1, W2, out, logits=None, expert_bi
                     W2_scales, out]
     a.dtype, a.T, a.E, a.k, a.H, a.I = dtype, T, E, k, H, I
     a.renormalize = int(renormalize)
-    a.flags = (MOE_FWD_HOST_IO if host_io else 0) | (MOE_FWD_GATHER if gather else 0)
+    a.flags = ((MOE_FWD_HOST_IO if host_io else 0) | (MOE_FWD_GATHER if gather else 0) |
+               (MOE_FWD_FUSED_COMBINE if fused_combine else 0))
     a.logits, a.expert_bias, a.sentinel_mask = _p(logits), _p(expert_bias), _p(sentinel_mask)
     a.topk_ids, a.topk_w = _p(topk_ids), _p(topk_w)
     a.x, a.W1, a.W1_scales, a.W2, a.W2_scales, a.out = (_p(x), _p(W1), _p(W1_scales), _p(W2),

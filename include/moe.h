@@ -300,6 +300,31 @@ moe_status_t moe_grouped_gemm_gather(moe_dtype_t dtype, const void* x, const flo
                                      float* C_scales, moe_stream_t stream);
 
 /*
+ * moe_grouped_gemm_combine -- the down grouped GEMM with the weighted combine
+ * folded into its epilogue (the fused pipeline of section 1 of the
+ * LlamaFactory write-up: group_gemm_same_nk (fc2) -> moe_gather), bf16 only.
+ * Computes Y2 = moe_grouped_gemm(h, W2, MOE_EPI_STORE) and, in the same
+ * kernel, out = moe_combine(Y2, topk_ids, topk_w, row_pos) -- bit for bit the
+ * two-call results.  After a CTA has stored its rows of a tile, each row's
+ * token bumps a counter per (token, 128-feature block); the CTA that stores
+ * the last of a token's live slots for a block sums that token's rows of the
+ * block, in slot order, with moe_combine's arithmetic.  Tokens whose slots
+ * are all sentinels get zero rows.  Y2 is still written (its rows are the
+ * inputs of the sums); only the separate combine launch is saved.
+ * h bf16 [M_cap, I]; W2 bf16 [E, H, I]; offsets [E+1]; topk_ids int32 [T, k]
+ * and topk_w fp32 [T, k] as given to moe_combine; sorted_rows, row_pos int32
+ * [T*k] from moe_route_sort; Y2 bf16 [M_cap, H]; out bf16 [T, H];
+ * ws: moe_grouped_gemm_combine_workspace_size(T, H) bytes of counters,
+ * cleared by the call.  Limits: those of moe_grouped_gemm (bf16, store) and
+ * moe_combine; T*k <= M_cap.
+ */
+size_t moe_grouped_gemm_combine_workspace_size(int T, int H);
+moe_status_t moe_grouped_gemm_combine(const void* h, const void* W2, const int32_t* offsets, int E, int M_cap,
+                                      int H, int I, const int32_t* topk_ids, const float* topk_w,
+                                      const int32_t* sorted_rows, const int32_t* row_pos, int T, int k, void* Y2,
+                                      void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Gradients of the bf16 grouped GEMM C[p, n] = sum_c A[p, c] * B[e, n, c]
  * (rows p of expert e; moe_grouped_gemm with MOE_EPI_STORE), for training
  * ("Mixture of Experts in transformers": MoE training on grouped GEMMs;
@@ -404,6 +429,10 @@ moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* t
                               GEMM fetches its rows four at a time, for every
                               column tile).  Ignored when H * element size is
                               not a multiple of 128. */
+#define MOE_FWD_FUSED_COMBINE 4u /* bf16: fold the weighted combine into the
+                              down GEMM (moe_grouped_gemm_combine instead of
+                              moe_grouped_gemm + moe_combine): same results,
+                              bit for bit.  Ignored for FP8. */
 
 /*
  * moe_forward -- the whole expert layer on one stream, in the order of the
