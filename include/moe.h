@@ -214,6 +214,9 @@ moe_status_t moe_ep_local_ids(const int32_t* topk_ids, int T, int k, int E_globa
  * nearest-even e4m3, saturating at +-448).
  * x bf16 [M, K]; q uint8 [M, K]; scales fp32 [M, K/128] (row-major).
  * Limits: M >= 1, K a positive multiple of 128.
+ * These scales are token-major, while moe_grouped_gemm reads its A scales
+ * group-major ([K/128, M_cap]): quantised tokens reach the GEMM through
+ * moe_permute, which moves each row's scales into that layout.
  */
 moe_status_t moe_act_quant_fp8(const void* x, int M, int K, uint8_t* q, float* scales,
                                moe_stream_t stream);
