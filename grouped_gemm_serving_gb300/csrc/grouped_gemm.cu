@@ -21,10 +21,11 @@
 // token rows (32 KB per k-block, six deep; seven for the store epilogue);
 // the even CTA issues the MMAs for both and commits to both CTAs' barriers;
 // each CTA's accumulator holds its weight rows x all tokens of the tile.
-// SwiGLU: a CTA's weight rows are 64 gate rows followed by the same 64 up
-// rows, so the epilogue warp pair that holds a feature's gate and up rows
-// swaps half of each 32-token chunk through shared memory and both compute
-// silu(g) * u.
+// SwiGLU: a CTA's 128 weight rows are its 64 features' gate and up rows,
+// interleaved in groups of 8 (8 gate rows, the same 8 up rows, ...), so a
+// feature's gate and up accumulators sit 8 lanes apart in one warp: the two
+// lanes swap half of each 32-token chunk with one shuffle per token and
+// both compute silu(g) * u.
 //
 // FP8 (and gathered A): single CTAs, 128 rows (tokens) x 256 columns
 // (weights), 48 KB per k-block, four deep.  Each 128-wide k-block is an exact
@@ -156,9 +157,6 @@ struct alignas(16) Shared {
     uint64_t xbar[2];  // amax exchange of the quantising epilogue
     uint64_t mma_done;
     uint64_t cbar;     // fused combine: every epilogue thread has stored its rows of the tile
-    // swapped SwiGLU: per epilogue warp pair, channel 0 carries gate values to
-    // the up warp and channel 1 up values to the gate warp (half a chunk each)
-    uint64_t xfull[4][2], xempty[4][2];
     uint32_t tmem_base;
     int abort_flag;
     int valid;
@@ -168,10 +166,7 @@ struct alignas(16) Aux {
     int kpre[kMaxE + 1];    // weight-gradient mode: exclusive prefix of k-blocks
     alignas(16) int gtok[kGatherWarps][BM];  // gathered A: each issuing warp's copy of the tile's tokens
     float amax_x[2][2][BM];  // quantising epilogue
-    union {
-        float scale_ring[kScaleRing * 3 * kEpiThreads];  // FP8 block scales in flight
-        float xch[4][2][16 * 32];                       // swapped SwiGLU exchange
-    };
+    float scale_ring[kScaleRing * 3 * kEpiThreads];  // FP8 block scales in flight
 };
 // The Aux block sits right after Shared; every kernel but the pair store
 // kernel allocates it, and only the code paths of those kernels reach it.
@@ -393,8 +388,8 @@ __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX3
                     moe::tma_load_3d_pair(sa + 8192, tmW, fb, f0 + 64, kc, ti.e);
                 } else if (EPI == EPI_STORE)
                     moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
-                else
-                    moe::tma_load_4d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 64, 0, ti.e);
+                else   // 8 groups of (8 gate rows, 8 up rows) of this CTA's 64 features
+                    moe::tma_load_5d_pair(sa, tmW, fb, kc, 0, 0, (ti.col0 + static_cast<int>(rank) * 64) / 8, ti.e);
                 if (nb <= 2) {
                     for (int b = 0; b < nb; ++b)
                         moe::tma_load_2d_pair(sb + b * 4096, tmX32, fb, kc, xrow + 32 * b);
@@ -738,8 +733,6 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int acc = 0, xsel = 0;
     uint32_t acc_phase = 0, xphase = 0;
-    const int xp = (q & 1) + 2 * hsel;   // swapped SwiGLU: warp pair (gate q, up q + 2) of this column half
-    uint32_t xph = 0;
     uint32_t cph = 0;                    // fused combine barrier phase
     const int KB = p.k_blocks;
 
@@ -778,27 +771,20 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                             if (col + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(__uint_as_float(v[j]));
                     }
                 } else {
-                    // gate warp (lanes 0-63) and up warp (lanes 64-127) of a
-                    // pair hold the same 32 features; each sends the other the
-                    // half of the chunk it does not compute, so the SwiGLU work
-                    // is spread evenly over the four SM sub-partitions
-                    const int r = q >= 2;                     // 0: gate warp, 1: up warp
-                    if (!moe::mbar_wait(bar(S.xempty[xp][r]), xph ^ 1u, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
-                    float* mine = aux(S).xch[xp][r];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = __uint_as_float(v[r ? j : 16 + j]);
-                    moe::mbar_arrive(bar(S.xfull[xp][r]));
-                    if (!moe::mbar_wait(bar(S.xfull[xp][r ^ 1]), xph, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
-                    const float* theirs = aux(S).xch[xp][r ^ 1];
+                    // lane l holds the gate (up, if bit 3 of l is set) row of
+                    // feature 16q + 8(l / 16) + l % 8; lanes l and l ^ 8 share
+                    // a feature.  The gate lane computes the chunk's first 16
+                    // tokens, the up lane the last 16, each receiving the
+                    // other's values for its tokens.
+                    const int r = (lane >> 3) & 1;            // 0: gate lane, 1: up lane
                     float h[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float o = theirs[j * 32 + lane];
-                        h[j] = r ? silu_mul(o, __uint_as_float(v[16 + j])) : silu_mul(__uint_as_float(v[j]), o);
+                        const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[16 + j]);
+                        const float o = __shfl_xor_sync(0xffffffffu, r ? lo : hi, 8);
+                        h[j] = r ? silu_mul(o, hi) : silu_mul(lo, o);
                     }
-                    moe::mbar_arrive(bar(S.xempty[xp][r ^ 1]));
-                    xph ^= 1u;
-                    const int f = ti.col0 + static_cast<int>(rank) * 64 + 32 * (q & 1) + lane;
+                    const int f = ti.col0 + static_cast<int>(rank) * 64 + 16 * q + 8 * (lane >> 4) + (lane & 7);
                     const int t0 = col + 16 * r;
                     if (f < p.out_cols) {
                         __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + t0) * p.out_cols + f;
@@ -1037,11 +1023,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         moe::mbar_init(bar(S.mma_done), 1);
         moe::mbar_init(bar(S.cbar), kEpiThreads);
-        for (int i = 0; i < 4; ++i)
-            for (int c = 0; c < 2; ++c) {
-                moe::mbar_init(bar(S.xfull[i][c]), 32);
-                moe::mbar_init(bar(S.xempty[i][c]), 32);
-            }
         S.abort_flag = 0;
         moe::fence_barrier_init();
     }
@@ -1177,7 +1158,7 @@ bool encode(CUtensorMap* map, bool fp8, const void* base, int rank, const cuuint
             const cuuint64_t* strides_bytes, const cuuint32_t* box) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
     return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
               static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes, box, estride,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1305,14 +1286,23 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(N) * K * esz};
         const cuuint32_t box[3] = {bk, swap ? 128u : BN, 1};   // swapped: 128 weight rows per CTA
         if (!encode(&tmB, fp8, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
+    } else if (swap) {
+        // [E, N/2/8, 2, 8, K] in memory order (expert, group of 8 features,
+        // gate/up, feature in group, k): one box holds 8 groups of 8 gate rows
+        // and the same 8 up rows; features past N/2 are out of bounds (zeros)
+        const cuuint64_t dims[5] = {static_cast<cuuint64_t>(K), 8, 2, static_cast<cuuint64_t>(half / 8),
+                                    static_cast<cuuint64_t>(E)};
+        const cuuint64_t strides[4] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(half) * K * esz,
+                                       static_cast<cuuint64_t>(8) * K * esz, static_cast<cuuint64_t>(N) * K * esz};
+        const cuuint32_t box[5] = {bk, 8, 2, 8, 1};
+        if (!encode(&tmB, fp8, B, 5, dims, strides, box)) return MOE_ERR_CUDA;
     } else {
         // [E, 2, N/2, K]: a gate box clips at N/2 instead of running into the up rows
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(half), 2,
                                     static_cast<cuuint64_t>(E)};
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(half) * K * esz,
                                        static_cast<cuuint64_t>(N) * K * esz};
-        // swapped: 64 gate rows and the same 64 up rows per box (per CTA)
-        const cuuint32_t box[4] = {bk, swap ? 64u : BN / 2, swap ? 2u : 1u, 1};
+        const cuuint32_t box[4] = {bk, BN / 2, 1u, 1};
         if (!encode(&tmB, fp8, B, 4, dims, strides, box)) return MOE_ERR_CUDA;
     }
 
