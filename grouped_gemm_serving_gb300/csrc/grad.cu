@@ -9,8 +9,10 @@
 //   wgrad  dB[e, n, c] = sum over expert e's rows of dC[p, n] A[p, c]: dC and A
 //          are transposed so that each expert's rows run along the contraction
 //          dimension from a 64-aligned start, zero-padded to whole 64-element
-//          k-blocks; then the grouped GEMM's weight-gradient mode walks each
-//          expert's own k-blocks (tcgen05, TMEM accumulators, TMA).
+//          k-blocks; then the grouped GEMM's weight-gradient kernel walks each
+//          expert's own k-blocks on CTA pairs (tcgen05 cta_group::2, the
+//          transposed A as the MMA's 256 rows and the transposed dC's rows as
+//          its columns, TMEM accumulators, TMA).
 // The padded layout is computed on the device from offsets: no host
 // synchronisation.
 #include <climits>

@@ -127,11 +127,12 @@ struct Params {
     const uint8_t* gx;
     const int32_t* sorted_rows;
     int T, topk;
-    // weight-gradient mode (single CTA, bf16 store): A is [wg_rows, P] and B
-    // [N, P], both with each expert's rows laid out along P from a 64-aligned
-    // start, zero-padded; expert e's tile rows are all wg_rows rows and its K
-    // range its own k-blocks; the output is [E, wg_rows, N].
-    int wg, wg_rows;
+    // weight-gradient kernel (WG: pair, bf16 store): the "weights" are
+    // [out_cols, P] and the "tokens" [wg_rows, P], both with each expert's
+    // rows laid out along P from a 64-aligned start, zero-padded; every
+    // expert has all wg_rows x out_cols output tiles over its own k-blocks;
+    // the output is [E, wg_rows, out_cols].
+    int wg_rows;
     // swapped store tiles only: the weights are MN-major, B [E, K, N] with
     // the N output features contiguous (the data gradient reads the forward
     // weights [E, N_fwd, K_fwd] in place this way)
@@ -163,7 +164,6 @@ struct alignas(16) Shared {
     int prefix[kMaxE + 1];  // exclusive prefix over experts of row-tile counts
 };
 struct alignas(16) Aux {
-    int kpre[kMaxE + 1];    // weight-gradient mode: exclusive prefix of k-blocks
     alignas(16) int gtok[kGatherWarps][BM];  // gathered A: each issuing warp's copy of the tile's tokens
     float amax_x[2][2][BM];  // quantising epilogue
     float scale_ring[kScaleRing * 3 * kEpiThreads];  // FP8 block scales in flight
@@ -172,9 +172,6 @@ struct alignas(16) Aux {
 // kernel allocates it, and only the code paths of those kernels reach it.
 __device__ __forceinline__ Aux& aux(Shared& S) {
     return *reinterpret_cast<Aux*>(reinterpret_cast<uint8_t*>(&S) + sizeof(Shared));
-}
-__device__ __forceinline__ const Aux& aux(const Shared& S) {
-    return *reinterpret_cast<const Aux*>(reinterpret_cast<const uint8_t*>(&S) + sizeof(Shared));
 }
 
 template <bool PAIR, int EPI>
@@ -193,28 +190,40 @@ struct Tile {
     int kb0, nkb;  // the tile's k-blocks: [kb0, kb0 + nkb)
 };
 
-template <bool SWAP>
+// Weight gradient: every expert has the same wg_pair_mt(p) token tiles.
+__device__ __forceinline__ int wg_pair_mt(const Params& p) { return (p.wg_rows + BT - 1) / BT; }
+
+template <bool SWAP, bool WG = false>
 __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params& p) {
-    int lo = 0, hi = p.E;  // largest e < E with prefix[e] * n_tiles <= t
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (S.prefix[mid] * p.n_tiles <= t) lo = mid; else hi = mid;
+    static_assert(!WG || SWAP, "the weight gradient runs on CTA pairs");
+    int lo = 0, mt, local;
+    if (WG) {
+        // every expert has mt x n_tiles tiles; S.prefix is its k-block prefix
+        mt = wg_pair_mt(p);
+        lo = t / (mt * p.n_tiles);
+        local = t - lo * mt * p.n_tiles;
+    } else {
+        int hi = p.E;  // largest e < E with prefix[e] * n_tiles <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (S.prefix[mid] * p.n_tiles <= t) lo = mid; else hi = mid;
+        }
+        mt = S.prefix[lo + 1] - S.prefix[lo];
+        local = t - S.prefix[lo] * p.n_tiles;
     }
-    const int mt = S.prefix[lo + 1] - S.prefix[lo];
-    const int local = t - S.prefix[lo] * p.n_tiles;
     Tile ti;
     ti.e = lo;
     ti.row_end = p.offsets[lo + 1];
     ti.kb0 = 0;
     ti.nkb = p.k_blocks;
-    if (!SWAP && p.wg) {
-        // weight gradient: every expert has the same output row tiles; its
-        // K range is its own zero-padded run of k-blocks
-        ti.row0 = (local % mt) * BM;
+    if (WG) {
+        // weight gradient on a pair: the tokens are the wg_rows output rows
+        // in tiles of BT, the K range the expert's zero-padded k-blocks
+        ti.row0 = (local % mt) * BT;
+        ti.rows = min(BT, p.wg_rows - ti.row0);
         ti.row_end = p.wg_rows;
-        ti.rows = 0;
-        ti.kb0 = aux(S).kpre[lo];
-        ti.nkb = aux(S).kpre[lo + 1] - aux(S).kpre[lo];
+        ti.kb0 = S.prefix[lo];
+        ti.nkb = S.prefix[lo + 1] - S.prefix[lo];
     } else if (SWAP) {
         // an expert's tokens in mt tiles of equal size (a multiple of 32),
         // rather than full tiles and a small remainder that would still
@@ -301,7 +310,7 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
         const Tile ti = decode_tile<false>(t, S, p);
-        for (int kb = 0; kb < ti.nkb; ++kb) {
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
             const bool got = moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
@@ -310,13 +319,11 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
             const uint32_t fb = bar(S.full[stage]);
             const uint32_t sa = moe::smem_u32(stages + stage * Geo<false, EPI>::kStageBytes);
             const uint32_t sb = sa + kStageA;
-            const int kc = (ti.kb0 + kb) * (FP8 ? 128 : 64);
+            const int kc = kb * (FP8 ? 128 : 64);
             if (moe::elect_one()) {
                 moe::mbar_arrive_expect_tx(fb, Geo<false, EPI>::kStageBytes);
                 moe::tma_load_2d(sa, tmA, fb, kc, ti.row0);
-                if (EPI == EPI_STORE && p.wg) {
-                    moe::tma_load_2d(sb, tmB, fb, kc, ti.col0);
-                } else if (EPI == EPI_STORE) {
+                if (EPI == EPI_STORE) {
                     moe::tma_load_3d(sb, tmB, fb, kc, ti.col0, ti.e);
                 } else {
                     moe::tma_load_4d(sb, tmB, fb, kc, ti.col0, 0, ti.e);
@@ -357,19 +364,20 @@ __device__ __forceinline__ int tile_step() { return PAIR ? gridDim.x >> 1 : grid
 // map).  Tokens: one 128-row box (tmX128), or up to two 32-row boxes (tmX32)
 // for a half of at most 64 rows.  A TMA instruction costs the issuing thread
 // many cycles, so a k-block takes as few as possible.
-template <int EPI>
+template <int EPI, bool WG>
 __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX32, const CUtensorMap* tmW,
                               uint8_t* stages, Shared& S, const Params& p, int total, uint32_t rank) {
     int stage = 0;
     uint32_t phase = 0, issued = 0, issued_par = 0;
     bool ok = true;
     for (int t = tile_first<true>(); ok && t < total; t += tile_step<true>()) {
-        const Tile ti = decode_tile<true>(t, S, p);
+        const Tile ti = decode_tile<true, WG>(t, S, p);
         const int nh = swap_n(ti) / 2;                 // token rows in each CTA
         const int nb = (nh + 31) / 32;
         const int xbytes = nb <= 2 ? nb * 4096 : kStageB / 2;
         const int xrow = ti.row0 + static_cast<int>(rank) * nh;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int nkb = WG ? ti.nkb : p.k_blocks, kb0 = WG ? ti.kb0 : 0;
+        for (int kb = 0; kb < nkb; ++kb) {
             const bool got = moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
@@ -378,10 +386,13 @@ __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX3
             const uint32_t fb = moe::map_to_cta(bar(S.full[stage]), 0);
             const uint32_t sa = moe::smem_u32(stages + stage * Geo<true, EPI>::kStageBytes);
             const uint32_t sb = sa + kStageA;
-            const int kc = kb * 64;
+            const int kc = (kb0 + kb) * 64;
             if (moe::elect_one()) {
                 if (rank == 0) moe::mbar_arrive_expect_tx(bar(S.full[stage]), 2 * (kStageA + xbytes));
-                if (EPI == EPI_STORE && p.mn_a) {
+                if (WG) {
+                    // weight gradient: the "weights" are the transposed [out_cols, P] operand
+                    moe::tma_load_2d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128);
+                } else if (EPI == EPI_STORE && p.mn_a) {
                     // two 64-feature x 64-row swizzle atoms, 8 KB apart
                     const int f0 = ti.col0 + static_cast<int>(rank) * 128;
                     moe::tma_load_3d_pair(sa, tmW, fb, f0, kc, ti.e);
@@ -518,7 +529,7 @@ __device__ void producer_gather(const CUtensorMap* tmA, const CUtensorMap* tmB, 
     }
 }
 
-template <bool FP8, int EPI, bool SWAP>
+template <bool FP8, int EPI, bool SWAP, bool WG>
 __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int total, uint32_t tmem) {
     uint32_t idesc = moe::make_idesc(FP8 ? 0u : 1u, BM, BN);
     int stage = 0, acc = 0;
@@ -526,7 +537,7 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
     bool ok = true, issued = false;
     for (int t = tile_first<SWAP>(); ok && t < total; t += tile_step<SWAP>()) {
         if (SWAP) {
-            const int n = swap_n(decode_tile<true>(t, S, p));
+            const int n = swap_n(decode_tile<true, WG>(t, S, p));
             idesc = EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n) : moe::make_idesc(1u, 2 * BM, n);
         }
         if (!FP8) {
@@ -538,7 +549,7 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
         }
         // weight-gradient tiles of an expert without rows have no k-blocks:
         // the accumulator is committed untouched and the epilogue writes zeros
-        const int nkb = !SWAP && p.wg ? decode_tile<false>(t, S, p).nkb : p.k_blocks;
+        const int nkb = WG ? decode_tile<SWAP, WG>(t, S, p).nkb : p.k_blocks;
         for (int kb = 0; kb < nkb; ++kb) {
             if (FP8) {
                 const bool got = moe::mbar_wait(bar(S.acc_empty[acc]), acc_phase ^ 1u, &S.abort_flag, kWaitNs);
@@ -724,7 +735,7 @@ __device__ void fused_combine_empty_tokens(const Params& p) {
     }
 }
 
-template <bool FP8, int EPI, bool SWAP>
+template <bool FP8, int EPI, bool SWAP, bool WG>
 __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;               // TMEM lane quarter this warp may access
@@ -743,7 +754,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
         acc_empty_leader[1] = moe::map_to_cta(bar(S.acc_empty[1]), 0);
     }
     for (int t = tile_first<SWAP>(); t < total; t += tile_step<SWAP>()) {
-        const Tile ti = decode_tile<SWAP>(t, S, p);
+        const Tile ti = decode_tile<SWAP, WG>(t, S, p);
         const int row = ti.row0 + r;
         const bool live = row < ti.row_end;
         if (SWAP) {
@@ -752,14 +763,21 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             moe::tc_fence_after();
             const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
             const int ntok = swap_rows(ti);
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+            // weight gradient: expert e's output rows start at e * wg_rows
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
+                                 (WG ? static_cast<int64_t>(ti.e) * p.wg_rows * p.out_cols : 0);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 const int col = hsel * 128 + c * 32;
                 if (col >= ntok) break;                       // the same for the whole warp
                 uint32_t v[32];
-                moe::tmem_ld32(ta + col, v);
-                moe::tmem_ld_wait();
+                if (!WG || ti.nkb > 0) {
+                    moe::tmem_ld32(ta + col, v);
+                    moe::tmem_ld_wait();
+                } else {   // an expert without rows: its weight gradient is zero
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
                 if (EPI == EPI_STORE) {
                     // one output feature per lane; a warp store covers 64
                     // contiguous bytes of one token row
@@ -804,20 +822,13 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             if (!moe::mbar_wait(bar(S.acc_full[acc]), acc_phase, &S.abort_flag, kWaitNs)) { fail(S, p); return; }
             moe::tc_fence_after();
             const uint32_t ta = lane_base + static_cast<uint32_t>(acc * BN);
-            // weight gradient: expert e's output rows start at e * wg_rows
-            const int64_t orow_idx = p.wg ? static_cast<int64_t>(ti.e) * p.wg_rows + row : row;
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + orow_idx * p.out_cols;
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row) * p.out_cols;
             if (EPI == EPI_STORE) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t v[32];
-                    if (ti.nkb > 0) {
-                        moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
-                        moe::tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0u;
-                    }
+                    moe::tmem_ld32(ta + hsel * 128 + c * 32, v);
+                    moe::tmem_ld_wait();
                     if (live) store_bf16x32(orow, ti.col0 + hsel * 128 + c * 32, p.out_cols,
                                             reinterpret_cast<const float*>(v));
                 }
@@ -999,7 +1010,7 @@ __device__ void zero_sentinel_rows(const Params& p) {
     }
 }
 
-template <bool FP8, int EPI, bool SWAP>
+template <bool FP8, int EPI, bool SWAP, bool WG = false>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA128, const __grid_constant__ CUtensorMap tmA32,
@@ -1039,11 +1050,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (hi < lo) bad = 1;
                 constexpr int RT = SWAP ? BT : BM;   // rows of an expert per tile
                 mt[i] = hi > lo ? (hi - lo + RT - 1) / RT : 0;
-                if (!SWAP && p.wg) {   // every expert: all output row tiles; k-blocks of its rows
-                    mt[i] = (p.wg_rows + BM - 1) / BM;
-                    kbl[i] = hi > lo ? (hi - lo + 63) / 64 : 0;
-                    ksum += kbl[i];
-                }
+                if (WG) kbl[i] = hi > lo ? (hi - lo + 63) / 64 : 0;   // k-blocks of its rows
+                ksum += kbl[i];
                 sum += mt[i];
             }
         }
@@ -1058,13 +1066,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (lane >= off) incl += o;
         }
         int run = incl - sum;
+        if (!WG) {   // the weight gradient keeps its k-block prefix here instead
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane * 8 + i;
-            if (e < p.E) { S.prefix[e] = run; run += mt[i]; }
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane * 8 + i;
+                if (e < p.E) { S.prefix[e] = run; run += mt[i]; }
+            }
+            if (lane == 31) S.prefix[p.E] = incl;
         }
-        if (lane == 31) S.prefix[p.E] = incl;
-        if (!SWAP && p.wg) {
+        if (WG) {
             int kincl = ksum;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -1075,9 +1085,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int e = lane * 8 + i;
-                if (e < p.E) { aux(S).kpre[e] = krun; krun += kbl[i]; }
+                if (e < p.E) { S.prefix[e] = krun; krun += kbl[i]; }
             }
-            if (lane == 31) aux(S).kpre[p.E] = kincl;
+            if (lane == 31) S.prefix[p.E] = kincl;
         }
         if (lane == 0) {
             S.valid = !bad;
@@ -1107,15 +1117,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     else __syncthreads();
     moe::tc_fence_after();
     const uint32_t tmem = S.tmem_base;
-    const int total = S.prefix[p.E] * p.n_tiles;   // tiles (pair tiles when SWAP)
+    // tiles (pair tiles when SWAP)
+    const int total = WG ? p.E * wg_pair_mt(p) * p.n_tiles : S.prefix[p.E] * p.n_tiles;
 
     // FP8 promotion keeps 128 fp32 accumulators per epilogue thread: move
     // registers from warpgroup 0 (TMA, MMA) to the two epilogue warpgroups.
     // 128 * kRegsLow + 256 * kRegsHigh = 384 * 168, the launch allocation.
     if (warp >= 4) {
         if (FP8) moe::reg_alloc<kRegsHigh>();
-        epilogue<FP8, EPI, SWAP>(S, p, total, tmem, rank);
-        if (!p.wg) zero_sentinel_rows<EPI>(p);
+        epilogue<FP8, EPI, SWAP, WG>(S, p, total, tmem, rank);
+        if (!WG) zero_sentinel_rows<EPI>(p);
         if (SWAP && EPI == EPI_STORE && p.fc) fused_combine_empty_tokens(p);
     } else {
         if (FP8) moe::reg_dealloc<kRegsLow>();
@@ -1123,10 +1134,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             producer_gather<FP8, EPI>(&tmA, &tmB, stages, S, p, total, warp == 0 ? 0 : warp - 1);
             __syncwarp();
         } else if (warp == 0) {
-            if (SWAP) producer_swap<EPI>(&tmA128, &tmA32, &tmB, stages, S, p, total, rank);
+            if (SWAP) producer_swap<EPI, WG>(&tmA128, &tmA32, &tmB, stages, S, p, total, rank);
             else producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
         } else if (warp == 1) {
-            if (rank == 0) mma_issuer<FP8, EPI, SWAP>(stages, S, p, total, tmem);
+            if (rank == 0) mma_issuer<FP8, EPI, SWAP, WG>(stages, S, p, total, tmem);
         }
     }
     moe::tc_fence_before();
@@ -1165,10 +1176,10 @@ bool encode(CUtensorMap* map, bool fp8, const void* base, int rank, const cuuint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, int EPI, bool SWAP = false>
+template <bool FP8, int EPI, bool SWAP = false, bool WG = false>
 moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA128,
                     const CUtensorMap& tmA32, const Params& p, cudaStream_t s) {
-    auto kern = grouped_gemm_kernel<FP8, EPI, SWAP>;
+    auto kern = grouped_gemm_kernel<FP8, EPI, SWAP, WG>;
     constexpr size_t kSmemBytes = smem_bytes<SWAP, EPI>();
     static int configured[64] = {0};
     int dev = 0;
@@ -1326,7 +1337,6 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     p.sorted_rows = sorted_rows;
     p.T = gx ? T : 0;
     p.topk = gx ? topk : 1;
-    p.wg = 0;
     p.wg_rows = 0;
     p.mn_a = weights_mn ? 1 : 0;
     p.fc = 0;
@@ -1370,23 +1380,30 @@ moe_status_t moe::dgrad_gemm(const void* dC, const void* B, const int32_t* offse
 
 moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, const int32_t* offsets, int E,
                              int M_cap, int N, int K, void* dB, cudaStream_t s) {
+    // dB[e] [N, K] = At_g[:, run_e] x Bt_g[:, run_e]^T over expert e's padded
+    // run of P.  Swapped operands on CTA pairs: Bt_g [K, P] supplies the
+    // MMA's M rows (the output features, 256 per pair tile), At_g [N, P] its
+    // N columns (the output rows, in tiles of up to 256).
     MOE_CHECK_ARG(At_g && Bt_g && offsets && dB && E >= 1 && E <= kMaxE && M_cap >= 1);
     MOE_CHECK_ARG(N >= 8 && N % 8 == 0 && K >= 8 && K % 8 == 0 && P >= 64 && P % 64 == 0);
     MOE_CHECK_ARG(P < INT_MAX && static_cast<int64_t>(E) * N < INT_MAX);
+    const int n_tiles = (K + kSwapFeatStore - 1) / kSwapFeatStore;
+    MOE_CHECK_ARG(static_cast<int64_t>(E) * ((N + BT - 1) / BT) * n_tiles < INT_MAX);
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
-    CUtensorMap tmA, tmB;
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
-        const cuuint32_t box[2] = {64, BM};
-        if (!encode(&tmA, false, At_g, 2, dims, strides, box)) return MOE_ERR_CUDA;
-    }
+    CUtensorMap tmW, tmX128, tmX32;
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(K)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
-        const cuuint32_t box[2] = {64, BN};
-        if (!encode(&tmB, false, Bt_g, 2, dims, strides, box)) return MOE_ERR_CUDA;
+        const cuuint32_t box[2] = {64, 128};   // 128 output features per CTA
+        if (!encode(&tmW, false, Bt_g, 2, dims, strides, box)) return MOE_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
+        const cuuint32_t box128[2] = {64, 128}, box32[2] = {64, 32};
+        if (!encode(&tmX128, false, At_g, 2, dims, strides, box128)) return MOE_ERR_CUDA;
+        if (!encode(&tmX32, false, At_g, 2, dims, strides, box32)) return MOE_ERR_CUDA;
     }
     Params p{};
     p.offsets = offsets;
@@ -1398,13 +1415,12 @@ moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, cons
     p.K = 64;
     p.half = 0;
     p.out_cols = K;
-    p.n_tiles = (K + BN - 1) / BN;
+    p.n_tiles = n_tiles;
     p.k_blocks = 0;
     p.nb_scale = 0;
     p.topk = 1;
-    p.wg = 1;
     p.wg_rows = N;
-    return launch<false, EPI_STORE>(tmA, tmB, tmA, tmA, p, s);
+    return launch<false, EPI_STORE, true, true>(tmX128, tmW, tmX128, tmX32, p, s);
 }
 
 extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,
