@@ -12,7 +12,7 @@ namespace moe {
 moe_status_t dgrad_gemm(const void* dC, const void* B, const int32_t* offsets, int E, int M_cap, int N, int K,
                         void* dA, cudaStream_t stream);
 
-// Launches the grouped GEMM in its weight-gradient mode (grouped_gemm.cu):
+// Launches the grouped GEMM's weight-gradient kernel on CTA pairs (grouped_gemm.cu):
 //   dB[e, n, c] = sum_j At_g[n, P_e + j] * Bt_g[c, P_e + j]
 // over expert e's zero-padded run [P_e, P_e + 64 * ceil(cnt_e / 64)) of the
 // transposed operands At_g bf16 [N, P] and Bt_g bf16 [K, P] (P a multiple of
