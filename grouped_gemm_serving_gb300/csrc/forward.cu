@@ -107,12 +107,14 @@ void* mapped_host_view(const void* p) {
 }
 
 // A second stream per device for the host-to-device copy of x, with the two
-// events that fork it from and join it to the caller's stream.  Created on
-// first use and kept for the life of the process; the mutex keeps the
-// record/wait sequences of concurrent calls from interleaving.
+// events that fork it from and join it to the caller's stream, and the event
+// that chains the kernels of successive host-I/O calls.  Created on first use
+// and kept for the life of the process; the mutex keeps the record/wait
+// sequences of concurrent calls from interleaving.
 struct CopyStream {
     cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, ready = nullptr;
+    cudaEvent_t fork = nullptr, ready = nullptr, chain = nullptr;
+    bool chained = false;   // chain holds the last call's kernels
     std::mutex mu;
 };
 constexpr int kMaxDevices = 64;
@@ -126,15 +128,17 @@ CopyStream* copy_stream() {
     std::lock_guard<std::mutex> lk(g_copy_init);
     if (!c.stream) {
         cudaStream_t st = nullptr;
-        cudaEvent_t a = nullptr, b = nullptr;
+        cudaEvent_t a = nullptr, b = nullptr, ch = nullptr;
         if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+            cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ch, cudaEventDisableTiming) != cudaSuccess) {
             (void)cudaGetLastError();
             return nullptr;
         }
         c.fork = a;
         c.ready = b;
+        c.chain = ch;
         c.stream = st;
     }
     return &c;
@@ -172,14 +176,16 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
     bool copy_out = false;
     CopyStream* cs = nullptr;
     std::unique_lock<std::mutex> cs_lock;
+    bool capturing = false;
     if (host_io) {
         // x (the large input) is copied in on a second stream while the
         // logits are copied and the batch routed on `stream`; the caller's
         // stream waits for x before the first kernel that reads it.  The
-        // output of a pinned `out` is written in place by the combine;
-        // pageable output memory gets a staged copy.  (Kernels reading pinned
-        // inputs over the host link in place were slower than the copy
-        // engine; writing the output in place was faster than a copy.)
+        // output of a pinned `out` is written in place by the combine (unless
+        // MOE_FWD_STAGED_OUT); pageable output memory gets a staged copy.
+        // (Kernels reading pinned inputs over the host link in place were
+        // slower than the copy engine; for one call at a time, writing the
+        // output in place was faster than a copy.)
         cs = copy_stream();
         if (!cs) return MOE_ERR_CUDA;
         cs_lock = std::unique_lock<std::mutex>(cs->mu);
@@ -196,7 +202,15 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
                                            cudaMemcpyHostToDevice, s));
             logits = ld;
         }
-        if (void* ov = mapped_host_view(a->out)) {
+        // the kernels of host-I/O calls run in call order: this call's wait
+        // for the previous call's (which may be on another stream), after the
+        // copies above so that they do not wait for them
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        MOE_CHECK_CUDA(cudaStreamIsCapturing(s, &cap));
+        capturing = cap != cudaStreamCaptureStatusNone;
+        if (!capturing && cs->chained) MOE_CHECK_CUDA(cudaStreamWaitEvent(s, cs->chain, 0));
+        void* ov = (a->flags & MOE_FWD_STAGED_OUT) ? nullptr : mapped_host_view(a->out);
+        if (ov) {
             out = ov;
         } else {
             out = base + l.out_dev;
@@ -212,10 +226,7 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
     MOE_TRY(moe_route_sort(logits, a->expert_bias, a->sentinel_mask, ids, w, T, E, k, a->renormalize,
                            sorted_rows, row_pos, offsets, base + l.route,
                            moe_route_sort_workspace_size(T, E, k), stream));
-    if (cs) {   // x has arrived before anything reads it
-        MOE_CHECK_CUDA(cudaStreamWaitEvent(s, cs->ready, 0));
-        cs_lock.unlock();
-    }
+    if (cs) MOE_CHECK_CUDA(cudaStreamWaitEvent(s, cs->ready, 0));   // x has arrived before anything reads it
     void* y2 = base + l.y2;
     if (!fp8) {
         void* h = base + l.h;
@@ -256,6 +267,13 @@ extern "C" moe_status_t moe_forward(const moe_forward_args* a, void* ws, size_t 
                                  MOE_EPI_STORE, y2, nullptr, stream));
     }
     if (fp8 || !(a->flags & MOE_FWD_FUSED_COMBINE)) MOE_TRY(moe_combine(y2, ids, w, row_pos, T, k, H, E, out, stream));
+    if (cs) {
+        if (!capturing) {
+            MOE_CHECK_CUDA(cudaEventRecord(cs->chain, s));
+            cs->chained = true;
+        }
+        cs_lock.unlock();
+    }
     if (copy_out)
         MOE_CHECK_CUDA(cudaMemcpyAsync(a->out, out, static_cast<size_t>(T) * H * 2, cudaMemcpyDeviceToHost, s));
     return MOE_OK;

@@ -24,6 +24,7 @@ MOE_DEVERR_NONE, MOE_DEVERR_OFFSETS, MOE_DEVERR_TIMEOUT, MOE_DEVERR_ROUTE = 0, 1
 MOE_FWD_HOST_IO = 1
 MOE_FWD_GATHER = 2
 MOE_FWD_FUSED_COMBINE = 4
+MOE_FWD_STAGED_OUT = 8
 
 
 class MoeError(RuntimeError):
@@ -274,7 +275,8 @@ def route_sort_t(E: int, k: int, *, logits=None, expert_bias=None, sentinel_mask
 
 def forward_args(*, dtype, T, E, k, H, I, x, W1, W2, out, logits=None, expert_bias=None,
                  sentinel_mask=None, topk_ids=None, topk_w=None, W1_scales=None, W2_scales=None,
-                 renormalize=True, host_io=False, gather=False, fused_combine=False) -> ForwardArgs:
+                 renormalize=True, host_io=False, gather=False, fused_combine=False,
+                 staged_out=False) -> ForwardArgs:
     """Fill a ForwardArgs from tensors (or raw addresses); ``gather`` sets
     MOE_FWD_GATHER.  The returned struct keeps the given tensors alive for as
     long as it lives."""
@@ -284,7 +286,7 @@ def forward_args(*, dtype, T, E, k, H, I, x, W1, W2, out, logits=None, expert_bi
     a.dtype, a.T, a.E, a.k, a.H, a.I = dtype, T, E, k, H, I
     a.renormalize = int(renormalize)
     a.flags = ((MOE_FWD_HOST_IO if host_io else 0) | (MOE_FWD_GATHER if gather else 0) |
-               (MOE_FWD_FUSED_COMBINE if fused_combine else 0))
+               (MOE_FWD_FUSED_COMBINE if fused_combine else 0) | (MOE_FWD_STAGED_OUT if staged_out else 0))
     a.logits, a.expert_bias, a.sentinel_mask = _p(logits), _p(expert_bias), _p(sentinel_mask)
     a.topk_ids, a.topk_w = _p(topk_ids), _p(topk_w)
     a.x, a.W1, a.W1_scales, a.W2, a.W2_scales, a.out = (_p(x), _p(W1), _p(W1_scales), _p(W2),

@@ -419,11 +419,20 @@ moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* t
                               device, created on the first such call), so the
                               routing on `stream` overlaps its copy; `stream`
                               waits for it before x is read.  A pinned `out`
-                              is written in place by the combine kernel;
-                              pageable `out` gets a staged copy back.  The
+                              is written in place by the combine kernel
+                              (unless MOE_FWD_STAGED_OUT); pageable `out`
+                              gets a staged copy back.  The
                               results equal the device-buffer call's bit for
-                              bit.  Calls made under stream capture take the
-                              library's copy stream into the capture. */
+                              bit.  The kernels of host-I/O calls on one
+                              device run in call order: each call's first
+                              kernel waits for the previous call's last one,
+                              even on another stream (its copies do not), so a
+                              caller alternating two streams overlaps one
+                              batch's copies with its neighbours' kernels
+                              without those kernels sharing the SMs.  Calls
+                              made under stream capture take the library's
+                              copy stream into the capture and are not
+                              chained. */
 #define MOE_FWD_GATHER 2u  /* fold the scatter into the gate_up GEMM
                               (moe_grouped_gemm_gather instead of moe_permute
                               + moe_grouped_gemm): same results, bit for bit,
@@ -436,6 +445,16 @@ moe_status_t moe_combine(const void* Y2, const int32_t* topk_ids, const float* t
                               down GEMM (moe_grouped_gemm_combine instead of
                               moe_grouped_gemm + moe_combine): same results,
                               bit for bit.  Ignored for FP8. */
+#define MOE_FWD_STAGED_OUT 8u /* with MOE_FWD_HOST_IO: a pinned `out` is
+                              also written through the workspace and copied
+                              back with cudaMemcpyAsync on `stream` (the copy
+                              engine instead of the combine kernel writing
+                              host memory over the host link).  Slower for a
+                              single call; faster for callers that overlap
+                              batches on several streams, where the kernel
+                              writing host memory would hold SMs the other
+                              batch's kernels need.  Same results, bit for
+                              bit.  Ignored without MOE_FWD_HOST_IO. */
 
 /*
  * moe_forward -- the whole expert layer on one stream, in the order of the

@@ -39,8 +39,9 @@ def run_forward(moe, wl, x, W1, W2, W1s=None, W2s=None, host_io=False, logits=No
     ids = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
     if host_io:
-        # pinned buffers are read and written in place by the kernels;
-        # pageable ones are staged through the workspace by the library
+        # a pinned output is written in place by the combine (or, with
+        # MOE_FWD_STAGED_OUT, copied back like a pageable one); inputs are
+        # copied in through the workspace
         pin = (lambda t: t.pin_memory()) if host_io != "pageable" else (lambda t: t.clone())
         xin = pin(torch.from_numpy(x.view(np.int16)))
         lin = pin(torch.from_numpy(logits))
@@ -52,7 +53,7 @@ def run_forward(moe, wl, x, W1, W2, W1s=None, W2s=None, host_io=False, logits=No
                          I=wl.I, x=xin, W1=W1, W2=W2, W1_scales=W1s, W2_scales=W2s, out=out, logits=lin,
                          expert_bias=None if bias is None else dev(bias),
                          sentinel_mask=None if mask is None else dev(mask), topk_ids=ids, topk_w=w,
-                         renormalize=wl.renormalize, host_io=bool(host_io))
+                         renormalize=wl.renormalize, host_io=bool(host_io), staged_out=host_io == "pinned-staged")
     nbytes = moe.moe_forward_workspace_size(a)
     assert nbytes > 0
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
@@ -101,7 +102,7 @@ def test_forward_fp8(moe, wl):
     assert err.max() <= TOL["fp8"], err.max()
 
 
-@pytest.mark.parametrize("memory", ["pinned", "pageable"])
+@pytest.mark.parametrize("memory", ["pinned", "pinned-staged", "pageable"])
 def test_forward_host_io_equals_device_path(moe, memory):
     wl = LAYERS[1]
     x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
@@ -114,7 +115,7 @@ def test_forward_host_io_equals_device_path(moe, memory):
     assert np.array_equal(y_dev, y_again)                     # bit-reproducible
 
 
-@pytest.mark.parametrize("memory", ["pinned", "pageable"])
+@pytest.mark.parametrize("memory", ["pinned", "pinned-staged", "pageable"])
 def test_fp8_forward_host_io_equals_device_path(moe, memory):
     wl = synth.Workload("fp8-host-io", T=150, E=8, k=2, H=256, I=256, n_sentinel=9, dtype="fp8")
     x, W1, W2 = synth.hidden_states(wl), synth.expert_weights(wl, "w1"), synth.expert_weights(wl, "w2")
@@ -177,3 +178,46 @@ def test_forward_is_bit_reproducible(moe, fp8):
         assert np.array_equal(y.view(np.uint32), runs[0][0].view(np.uint32))
         assert np.array_equal(ids, runs[0][1])
         assert np.array_equal(w.view(np.uint32), runs[0][2].view(np.uint32))
+
+
+@pytest.mark.parametrize("staged_out", [False, True])
+def test_host_io_calls_alternating_two_streams(moe, staged_out):
+    """A serving loop through the host path: batches alternate over two streams
+    (a workspace and pinned buffers each), which the library chains in call
+    order.  Every batch's output equals the device-buffer call on its input."""
+    wl = LAYERS[1]
+    W1, W2 = dev_bf16(synth.expert_weights(wl, "w1")), dev_bf16(synth.expert_weights(wl, "w2"))
+    logits = synth.router_logits(wl)
+    xs = [synth.hidden_states(wl)]
+    xs.append((xs[0].view(np.uint16) ^ np.uint16(0x8000)).view(xs[0].dtype))   # the same batch negated
+    want = [run_forward(moe, wl, x, W1, W2, logits=logits)[0] for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs, args, wss = [], [], []
+    for i in range(2):
+        x_pin = torch.from_numpy(xs[i].view(np.int16)).pin_memory()
+        l_pin = torch.from_numpy(logits).pin_memory()
+        out = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+        a = moe.forward_args(dtype=moe.MOE_BF16, T=wl.T, E=wl.E, k=wl.k, H=wl.H, I=wl.I, x=x_pin, W1=W1, W2=W2,
+                             out=out, logits=l_pin, renormalize=wl.renormalize, host_io=True, staged_out=staged_out)
+        n = moe.moe_forward_workspace_size(a)
+        outs.append(out)
+        args.append(a)
+        wss.append((torch.empty(n, dtype=torch.uint8, device="cuda"), n))
+    torch.cuda.synchronize()
+    for b in range(6):
+        i = b & 1
+        outs[i].fill_(11)
+        with torch.cuda.stream(streams[i]):
+            moe.moe_forward(args[i], *wss[i])
+        streams[i].synchronize()
+        got = outs[i].view(torch.bfloat16).float().numpy()
+        assert np.array_equal(got, want[i]), b
+    # now back to back, without waiting in between
+    for b in range(6):
+        i = b & 1
+        with torch.cuda.stream(streams[i]):
+            moe.moe_forward(args[i], *wss[i])
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    for i in range(2):
+        assert np.array_equal(outs[i].view(torch.bfloat16).float().numpy(), want[i])
