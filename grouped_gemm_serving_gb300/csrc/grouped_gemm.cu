@@ -184,6 +184,14 @@ static_assert(smem_bytes<false, EPI_STORE>() <= 227 * 1024 && smem_bytes<false, 
                   smem_bytes<true, EPI_STORE>() <= 227 * 1024 && smem_bytes<true, EPI_SWIGLU>() <= 227 * 1024,
               "shared memory per CTA");
 
+// Tensor maps over the token operand of the swapped kernels with boxes of
+// 16, 32, .., 128 rows: a CTA's half of a token tile is one box of exactly
+// its height.
+constexpr int kTokenMaps = 8;
+struct TokenMaps {
+    CUtensorMap m[kTokenMaps];
+};
+
 struct Tile {
     int e, row0, row_end, col0;
     int rows;  // swapped: token rows of this tile (<= BT)
@@ -359,22 +367,22 @@ __device__ __forceinline__ int tile_step() { return PAIR ? gridDim.x >> 1 : grid
 // Producer with swapped operands on a CTA pair (bf16).  Per k-block each CTA
 // loads its 128 weight rows into the A region and its N/2 token rows into
 // the B region, all counted on the leading CTA's full barrier (the leader
-// posts both CTAs' bytes).  SwiGLU: CTA r's weight rows are gate rows
-// col0+64r .. +63 followed by the same up rows (one box of the [E, 2, N/2, K]
-// map).  Tokens: one 128-row box (tmX128), or up to two 32-row boxes (tmX32)
-// for a half of at most 64 rows.  A TMA instruction costs the issuing thread
-// many cycles, so a k-block takes as few as possible.
+// posts both CTAs' bytes).  SwiGLU: CTA r's 128 weight rows are its 64
+// features' gate and up rows, interleaved in groups of 8 (one 5-D box).
+// Tokens: one box of exactly the tile's N/2 rows (a multiple of 16, one
+// tensor map per height).  A TMA instruction costs the issuing thread many
+// cycles, so a k-block takes as few as possible.
 template <int EPI, bool WG>
-__device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX32, const CUtensorMap* tmW,
+__device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
                               uint8_t* stages, Shared& S, const Params& p, int total, uint32_t rank) {
     int stage = 0;
     uint32_t phase = 0, issued = 0, issued_par = 0;
     bool ok = true;
     for (int t = tile_first<true>(); ok && t < total; t += tile_step<true>()) {
         const Tile ti = decode_tile<true, WG>(t, S, p);
-        const int nh = swap_n(ti) / 2;                 // token rows in each CTA
-        const int nb = (nh + 31) / 32;
-        const int xbytes = nb <= 2 ? nb * 4096 : kStageB / 2;
+        const int nh = swap_n(ti) / 2;                 // token rows in each CTA: 16 .. 128
+        const CUtensorMap* tmXh = &tmX->m[nh / 16 - 1];
+        const int xbytes = nh * 128;
         const int xrow = ti.row0 + static_cast<int>(rank) * nh;
         const int nkb = WG ? ti.nkb : p.k_blocks, kb0 = WG ? ti.kb0 : 0;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -401,12 +409,7 @@ __device__ void producer_swap(const CUtensorMap* tmX128, const CUtensorMap* tmX3
                     moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
                 else   // 8 groups of (8 gate rows, 8 up rows) of this CTA's 64 features
                     moe::tma_load_5d_pair(sa, tmW, fb, kc, 0, 0, (ti.col0 + static_cast<int>(rank) * 64) / 8, ti.e);
-                if (nb <= 2) {
-                    for (int b = 0; b < nb; ++b)
-                        moe::tma_load_2d_pair(sb + b * 4096, tmX32, fb, kc, xrow + 32 * b);
-                } else {
-                    moe::tma_load_2d_pair(sb, tmX128, fb, kc, xrow);
-                }
+                moe::tma_load_2d_pair(sb, tmXh, fb, kc, xrow);
             }
             __syncwarp();
             issued |= 1u << stage;
@@ -1013,7 +1016,7 @@ __device__ void zero_sentinel_rows(const Params& p) {
 template <bool FP8, int EPI, bool SWAP, bool WG = false>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmA128, const __grid_constant__ CUtensorMap tmA32,
+                    const __grid_constant__ TokenMaps tmX,
                     const Params p) {
     static_assert(!(SWAP && FP8), "swapped operands are a bf16 path");
     const uint32_t rank = SWAP ? moe::cluster_ctarank() : 0;   // 0 leads a pair
@@ -1097,8 +1100,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         moe::prefetch_tensormap(&tmA);
         moe::prefetch_tensormap(&tmB);
         if (SWAP) {
-            moe::prefetch_tensormap(&tmA128);
-            moe::prefetch_tensormap(&tmA32);
+            for (int j = 0; j < kTokenMaps; ++j) moe::prefetch_tensormap(&tmX.m[j]);
         }
     }
     __syncthreads();
@@ -1134,7 +1136,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             producer_gather<FP8, EPI>(&tmA, &tmB, stages, S, p, total, warp == 0 ? 0 : warp - 1);
             __syncwarp();
         } else if (warp == 0) {
-            if (SWAP) producer_swap<EPI, WG>(&tmA128, &tmA32, &tmB, stages, S, p, total, rank);
+            if (SWAP) producer_swap<EPI, WG>(&tmX, &tmB, stages, S, p, total, rank);
             else producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
         } else if (warp == 1) {
             if (rank == 0) mma_issuer<FP8, EPI, SWAP, WG>(stages, S, p, total, tmem);
@@ -1176,9 +1178,18 @@ bool encode(CUtensorMap* map, bool fp8, const void* base, int rank, const cuuint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [rows, K] (dims/strides as for encode) with boxes of 64 x 16(j + 1) rows.
+bool encode_token_maps(TokenMaps* t, const void* base, const cuuint64_t* dims, const cuuint64_t* strides) {
+    for (int j = 0; j < kTokenMaps; ++j) {
+        const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(16 * (j + 1))};
+        if (!encode(&t->m[j], false, base, 2, dims, strides, box)) return false;
+    }
+    return true;
+}
+
 template <bool FP8, int EPI, bool SWAP = false, bool WG = false>
-moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmA128,
-                    const CUtensorMap& tmA32, const Params& p, cudaStream_t s) {
+moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const TokenMaps& tmX, const Params& p,
+                    cudaStream_t s) {
     auto kern = grouped_gemm_kernel<FP8, EPI, SWAP, WG>;
     constexpr size_t kSmemBytes = smem_bytes<SWAP, EPI>();
     static int configured[64] = {0};
@@ -1194,7 +1205,7 @@ moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtens
     if (SWAP) grid &= ~1;   // whole CTA pairs
     if (grid <= 0) return MOE_ERR_CUDA;
     if (!SWAP) {
-        kern<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmA128, tmA32, p);
+        kern<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmX, p);
         MOE_CHECK_LAUNCH();
         return MOE_OK;
     }
@@ -1210,7 +1221,7 @@ moe_status_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtens
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmA128, tmA32, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmX, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return MOE_ERR_CUDA;
     }
@@ -1273,17 +1284,16 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     if (!err) return MOE_ERR_CUDA;
 
     const cuuint32_t bk = 128 / esz;  // elements in a 128-byte k-block row
-    CUtensorMap tmA, tmB, tmA128, tmA32;
+    CUtensorMap tmA, tmB;
+    TokenMaps tmX{};
     {
-        // permuted A: 128-row tiles (swapped: token tiles in boxes of 256,
-        // 128 or 32 rows); gathered A: x [T, K] read a row at a time
+        // permuted A: 128-row tiles (swapped: token halves in boxes of 16 ..
+        // 128 rows); gathered A: x [T, K] read a row at a time
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(gx ? T : M_cap)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * esz};
         const cuuint32_t box[2] = {bk, gx ? 1u : swap ? static_cast<cuuint32_t>(BT) : static_cast<cuuint32_t>(BM)};
         if (!encode(&tmA, fp8, A, 2, dims, strides, box)) return MOE_ERR_CUDA;
-        const cuuint32_t box128[2] = {bk, 128u}, box32[2] = {bk, 32u};
-        if (!encode(&tmA128, fp8, A, 2, dims, strides, box128)) return MOE_ERR_CUDA;
-        if (!encode(&tmA32, fp8, A, 2, dims, strides, box32)) return MOE_ERR_CUDA;
+        if (swap && !encode_token_maps(&tmX, A, dims, strides)) return MOE_ERR_CUDA;
     }
     if (weights_mn) {
         if (fp8 || swiglu || gx) return MOE_ERR_UNSUPPORTED;
@@ -1355,16 +1365,16 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fp8) {
-        if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
-        if (epilogue == MOE_EPI_SWIGLU) return launch<true, EPI_SWIGLU>(tmA, tmB, tmA128, tmA32, p, s);
-        return launch<true, EPI_SWIGLU_Q>(tmA, tmB, tmA128, tmA32, p, s);
+        if (epilogue == MOE_EPI_STORE) return launch<true, EPI_STORE>(tmA, tmB, tmX, p, s);
+        if (epilogue == MOE_EPI_SWIGLU) return launch<true, EPI_SWIGLU>(tmA, tmB, tmX, p, s);
+        return launch<true, EPI_SWIGLU_Q>(tmA, tmB, tmX, p, s);
     }
     if (swap) {
-        if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE, true>(tmA, tmB, tmA128, tmA32, p, s);
-        return launch<false, EPI_SWIGLU, true>(tmA, tmB, tmA128, tmA32, p, s);
+        if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE, true>(tmA, tmB, tmX, p, s);
+        return launch<false, EPI_SWIGLU, true>(tmA, tmB, tmX, p, s);
     }
-    if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE>(tmA, tmB, tmA128, tmA32, p, s);
-    return launch<false, EPI_SWIGLU>(tmA, tmB, tmA128, tmA32, p, s);
+    if (epilogue == MOE_EPI_STORE) return launch<false, EPI_STORE>(tmA, tmB, tmX, p, s);
+    return launch<false, EPI_SWIGLU>(tmA, tmB, tmX, p, s);
 }
 
 }  // namespace
@@ -1391,7 +1401,8 @@ moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, cons
     MOE_CHECK_ARG(static_cast<int64_t>(E) * ((N + BT - 1) / BT) * n_tiles < INT_MAX);
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
-    CUtensorMap tmW, tmX128, tmX32;
+    CUtensorMap tmW;
+    TokenMaps tmX{};
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(K)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
@@ -1401,9 +1412,7 @@ moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, cons
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
-        const cuuint32_t box128[2] = {64, 128}, box32[2] = {64, 32};
-        if (!encode(&tmX128, false, At_g, 2, dims, strides, box128)) return MOE_ERR_CUDA;
-        if (!encode(&tmX32, false, At_g, 2, dims, strides, box32)) return MOE_ERR_CUDA;
+        if (!encode_token_maps(&tmX, At_g, dims, strides)) return MOE_ERR_CUDA;
     }
     Params p{};
     p.offsets = offsets;
@@ -1420,7 +1429,7 @@ moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, cons
     p.nb_scale = 0;
     p.topk = 1;
     p.wg_rows = N;
-    return launch<false, EPI_STORE, true, true>(tmX128, tmW, tmX128, tmX32, p, s);
+    return launch<false, EPI_STORE, true, true>(tmX.m[kTokenMaps - 1], tmW, tmX, p, s);
 }
 
 extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,
