@@ -16,9 +16,9 @@
 // bf16 (SWAP): swapped operands on CTA pairs (clusters of two, tcgen05
 // cta_group::2).  A pair tile is 256 weight rows (128 per CTA) x the tokens of
 // one token tile of one expert (up to 256, split equally within the expert,
-// the MMA's N rounded up to 32), so the tokens of an expert pad to a multiple
-// of 32 instead of 128.  Each CTA stages its 128 weight rows and half the
-// token rows (32 KB per k-block, six deep; seven for the store epilogue);
+// the MMA's N rounded up to 16), so the tokens of an expert pad to a multiple
+// of 16 instead of 128.  Each CTA stages its 128 weight rows and half the
+// token rows (up to 32 KB per k-block, six deep; seven for the store epilogue);
 // the even CTA issues the MMAs for both and commits to both CTAs' barriers;
 // each CTA's accumulator holds its weight rows x all tokens of the tile.
 // SwiGLU: a CTA's 128 weight rows are its 64 features' gate and up rows,
@@ -100,7 +100,7 @@ constexpr int kGatherWarps = 3; // warps 0, 2, 3 issue the row gathers of gather
 // Swapped operands on CTA pairs (bf16): the weights are the M = 256 rows of
 // a tcgen05 cta_group::2 MMA (128 per CTA) and an expert's tokens its N = up
 // to BT columns (N/2 rows in each CTA's shared memory), so a tile pads the
-// expert's rows to a multiple of 32 instead of 128, and each SM loads 32 KB
+// expert's rows to a multiple of 16 instead of 128, and each SM loads up to 32 KB
 // of operands per k-block instead of 48 KB.
 constexpr int BT = 256;
 constexpr int kSwapFeatSwiglu = 128;  // h features per pair tile (each CTA: 64 gate + 64 up rows)
@@ -185,9 +185,9 @@ static_assert(smem_bytes<false, EPI_STORE>() <= 227 * 1024 && smem_bytes<false, 
               "shared memory per CTA");
 
 // Tensor maps over the token operand of the swapped kernels with boxes of
-// 16, 32, .., 128 rows: a CTA's half of a token tile is one box of exactly
+// 8, 16, .., 128 rows: a CTA's half of a token tile is one box of exactly
 // its height.
-constexpr int kTokenMaps = 8;
+constexpr int kTokenMaps = 16;
 struct TokenMaps {
     CUtensorMap m[kTokenMaps];
 };
@@ -233,11 +233,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
         ti.kb0 = S.prefix[lo];
         ti.nkb = S.prefix[lo + 1] - S.prefix[lo];
     } else if (SWAP) {
-        // an expert's tokens in mt tiles of equal size (a multiple of 32),
+        // an expert's tokens in mt tiles of equal size (a multiple of 16),
         // rather than full tiles and a small remainder that would still
         // stream the whole weight tile
         const int cnt = ti.row_end - p.offsets[lo];
-        const int ts = ((cnt + mt - 1) / mt + 31) & ~31;
+        const int ts = ((cnt + mt - 1) / mt + 15) & ~15;
         ti.row0 = p.offsets[lo] + (local % mt) * ts;
         ti.rows = min(ts, ti.row_end - ti.row0);
     } else {
@@ -354,9 +354,10 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     __syncwarp();
 }
 
-// Token rows of a swapped tile (at most BT; the MMA's N is this rounded up to 32).
+// Token rows of a swapped tile (at most BT; the MMA's N is this rounded up to 16,
+// which cta_group::2 M = 256 MMAs allow).
 __device__ __forceinline__ int swap_rows(const Tile& ti) { return ti.rows; }
-__device__ __forceinline__ int swap_n(const Tile& ti) { return (ti.rows + 31) & ~31; }
+__device__ __forceinline__ int swap_n(const Tile& ti) { return (ti.rows + 15) & ~15; }
 
 // Tile loop bounds: a CTA pair walks the tile list as one unit.
 template <bool PAIR>
@@ -369,7 +370,7 @@ __device__ __forceinline__ int tile_step() { return PAIR ? gridDim.x >> 1 : grid
 // the B region, all counted on the leading CTA's full barrier (the leader
 // posts both CTAs' bytes).  SwiGLU: CTA r's 128 weight rows are its 64
 // features' gate and up rows, interleaved in groups of 8 (one 5-D box).
-// Tokens: one box of exactly the tile's N/2 rows (a multiple of 16, one
+// Tokens: one box of exactly the tile's N/2 rows (a multiple of 8, one
 // tensor map per height).  A TMA instruction costs the issuing thread many
 // cycles, so a k-block takes as few as possible.
 template <int EPI, bool WG>
@@ -380,8 +381,8 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
     bool ok = true;
     for (int t = tile_first<true>(); ok && t < total; t += tile_step<true>()) {
         const Tile ti = decode_tile<true, WG>(t, S, p);
-        const int nh = swap_n(ti) / 2;                 // token rows in each CTA: 16 .. 128
-        const CUtensorMap* tmXh = &tmX->m[nh / 16 - 1];
+        const int nh = swap_n(ti) / 2;                 // token rows in each CTA: 8 .. 128
+        const CUtensorMap* tmXh = &tmX->m[nh / 8 - 1];
         const int xbytes = nh * 128;
         const int xrow = ti.row0 + static_cast<int>(rank) * nh;
         const int nkb = WG ? ti.nkb : p.k_blocks, kb0 = WG ? ti.kb0 : 0;
@@ -1178,10 +1179,10 @@ bool encode(CUtensorMap* map, bool fp8, const void* base, int rank, const cuuint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 [rows, K] (dims/strides as for encode) with boxes of 64 x 16(j + 1) rows.
+// bf16 [rows, K] (dims/strides as for encode) with boxes of 64 x 8(j + 1) rows.
 bool encode_token_maps(TokenMaps* t, const void* base, const cuuint64_t* dims, const cuuint64_t* strides) {
     for (int j = 0; j < kTokenMaps; ++j) {
-        const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(16 * (j + 1))};
+        const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(8 * (j + 1))};
         if (!encode(&t->m[j], false, base, 2, dims, strides, box)) return false;
     }
     return true;
