@@ -143,16 +143,21 @@ def test_deterministic(moe):
 
 
 # bf16 runs with swapped operands on CTA pairs: an expert's tokens form
-# ceil(cnt/256) equal tiles rounded up to 32 rows.  Expert sizes around those
-# boundaries (1, 31-33, 255-257, 512-513 rows, several tiles) for both
-# epilogues, with an N tail and K not a multiple of the 64-element k-block.
-PAIR_COUNTS = [1, 31, 32, 33, 255, 256, 257, 512, 513, 700, 0, 1500]
+# ceil(cnt/256) equal tiles rounded up to 16 rows, each CTA loading half of a
+# tile (8 to 128 rows) as one box of that height.  Expert sizes around those
+# boundaries (1, 15-17, 31-33, 255-257, 512-513 rows, several tiles) for both
+# epilogues, with an N tail and K not a multiple of the 64-element k-block;
+# and one expert per box height (tiles of 16, 32, .., 256 rows).
+PAIR_COUNTS = [1, 15, 16, 17, 31, 32, 33, 255, 256, 257, 512, 513, 700, 0, 1500]
+BOX_COUNTS = [9, 17, 40, 50, 70, 90, 100, 120, 130, 150, 170, 180, 200, 220, 240, 250]
 
 
+@pytest.mark.parametrize("counts", ["boundaries", "box_heights"])
 @pytest.mark.parametrize("epi", ["store", "swiglu"])
-def test_bf16_token_tile_boundaries(moe, epi):
-    E = len(PAIR_COUNTS)
-    off = np.concatenate([[0], np.cumsum(PAIR_COUNTS)]).astype(np.int32)
+def test_bf16_token_tile_boundaries(moe, epi, counts):
+    counts = PAIR_COUNTS if counts == "boundaries" else BOX_COUNTS
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     live = int(off[-1])
     M_cap, K = live + 40, 200
     N = 392 if epi == "store" else 2 * 200
