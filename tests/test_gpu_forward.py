@@ -221,3 +221,41 @@ def test_host_io_calls_alternating_two_streams(moe, staged_out):
     assert moe.moe_get_device_error() == 0
     for i in range(2):
         assert np.array_equal(outs[i].view(torch.bfloat16).float().numpy(), want[i])
+
+
+@pytest.mark.parametrize("host_io", [False, True])
+def test_forward_captured_in_a_cuda_graph(moe, host_io):
+    """moe_forward enqueues no host synchronisation, so it can be captured
+    into a CUDA graph (the host path takes the library's copy stream into the
+    capture); replays give the eager call's output bit for bit."""
+    wl = LAYERS[1]
+    x = synth.hidden_states(wl)
+    W1, W2 = dev_bf16(synth.expert_weights(wl, "w1")), dev_bf16(synth.expert_weights(wl, "w2"))
+    logits = synth.router_logits(wl)
+    want, _, _ = run_forward(moe, wl, x, W1, W2, logits=logits)
+    if host_io:
+        xin = torch.from_numpy(x.view(np.int16)).pin_memory()
+        lin = torch.from_numpy(logits).pin_memory()
+        out = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    else:
+        xin, lin = dev_bf16(x), dev(logits)
+        out = torch.empty((wl.T, wl.H), dtype=torch.int16, device="cuda")
+    a = moe.forward_args(dtype=moe.MOE_BF16, T=wl.T, E=wl.E, k=wl.k, H=wl.H, I=wl.I, x=xin, W1=W1, W2=W2,
+                         out=out, logits=lin, renormalize=wl.renormalize, host_io=host_io)
+    n = moe.moe_forward_workspace_size(a)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        moe.moe_forward(a, ws, n)                     # warm-up outside the capture
+        with torch.cuda.graph(g, stream=side):
+            moe.moe_forward(a, ws, n)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        got = out.view(torch.bfloat16).float().cpu().numpy()
+        assert np.array_equal(got, want)
+    assert moe.moe_get_device_error() == 0
