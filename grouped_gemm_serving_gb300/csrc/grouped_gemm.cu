@@ -18,7 +18,7 @@
 // one token tile of one expert (up to 256, split equally within the expert,
 // the MMA's N rounded up to 16), so the tokens of an expert pad to a multiple
 // of 16 instead of 128.  Each CTA stages its 128 weight rows and half the
-// token rows (up to 32 KB per k-block, six deep; seven for the store epilogue);
+// token rows (up to 32 KB per k-block, seven deep);
 // the even CTA issues the MMAs for both and commits to both CTAs' barriers;
 // each CTA's accumulator holds its weight rows x all tokens of the tile.
 // SwiGLU: a CTA's 128 weight rows are its 64 features' gate and up rows,
@@ -85,13 +85,13 @@ constexpr int kStageB = BN * 128;
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SWIGLU_Q = 2 };
 
 // Stage ring: a single-CTA tile stages 128 A + 256 B rows (48 KB) four deep;
-// a CTA of a pair stages 128 + 128 rows (32 KB) six deep, or seven for the
-// store epilogue, which needs no shared memory beyond the ring and the
-// barriers (it allocates no Aux block, see smem_bytes).
+// a CTA of a pair stages up to 128 + 128 rows (32 KB) seven deep: its
+// epilogues need no shared memory beyond the ring and the barriers (pair
+// kernels allocate no Aux block, see smem_bytes).
 constexpr int kMaxStages = 7;
 template <bool PAIR, int EPI>
 struct Geo {
-    static constexpr int kStages = PAIR ? (EPI == EPI_STORE ? 7 : 6) : 4;
+    static constexpr int kStages = PAIR ? 7 : 4;
     static constexpr int kStageBytes = PAIR ? kStageA + kStageB / 2 : kStageA + kStageB;
 };
 constexpr int kMaxE = 256;
@@ -168,8 +168,8 @@ struct alignas(16) Aux {
     float amax_x[2][2][BM];  // quantising epilogue
     float scale_ring[kScaleRing * 3 * kEpiThreads];  // FP8 block scales in flight
 };
-// The Aux block sits right after Shared; every kernel but the pair store
-// kernel allocates it, and only the code paths of those kernels reach it.
+// The Aux block sits right after Shared; the single-CTA kernels allocate it,
+// and only their code paths reach it.
 __device__ __forceinline__ Aux& aux(Shared& S) {
     return *reinterpret_cast<Aux*>(reinterpret_cast<uint8_t*>(&S) + sizeof(Shared));
 }
@@ -177,7 +177,7 @@ __device__ __forceinline__ Aux& aux(Shared& S) {
 template <bool PAIR, int EPI>
 constexpr size_t smem_bytes() {
     using G = Geo<PAIR, EPI>;
-    constexpr bool with_aux = !(PAIR && EPI == EPI_STORE);
+    constexpr bool with_aux = !PAIR;
     return 1024 + static_cast<size_t>(G::kStages) * G::kStageBytes + sizeof(Shared) + (with_aux ? sizeof(Aux) : 0);
 }
 static_assert(smem_bytes<false, EPI_STORE>() <= 227 * 1024 && smem_bytes<false, EPI_SWIGLU_Q>() <= 227 * 1024 &&
