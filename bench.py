@@ -685,8 +685,9 @@ def grad_main(args, wl, synth, torch, moe):
         raise SystemExit("device error in the gradient bench")
     print(json.dumps({"metric": "grouped GEMM forward and gradients", "unit": "TFLOP/s",
                       "config": {"workload": wl.name, "live_rows": live, "l2": "flushed between timed calls",
-                                 "steps": args.steps, "note": "dgrad reads the weights in place; wgrad includes "
-                                 "the padded transposes of the activations and output gradients"},
+                                 "steps": args.steps, "note": "dgrad reads the weights in place; wgrad reads the "
+                                 "activations and output gradients in place and includes the copy of "
+                                 "each expert's partial last 64 rows"},
                       "peak": {"bf16_tflops": pk["bf16_tflops"], "kind": pk_kind}, "rows": rows}))
     return 0
 

@@ -388,6 +388,10 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, int M, int
 __host__ __device__ constexpr uint32_t make_idesc_a_mn(uint32_t ab_format, int M, int N) {
     return make_idesc(ab_format, M, N) | (1u << 15);
 }
+// The same with A and B read MN-major (bits 15 and 16, "transpose A/B").
+__host__ __device__ constexpr uint32_t make_idesc_ab_mn(uint32_t ab_format, int M, int N) {
+    return make_idesc(ab_format, M, N) | (1u << 15) | (1u << 16);
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

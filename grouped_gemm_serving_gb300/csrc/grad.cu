@@ -6,15 +6,14 @@
 //   dgrad  dA[p, c] = sum_n dC[p, n] B[e, n, c]: the grouped GEMM kernel with
 //          B read in place as an MN-major operand (the c features contiguous);
 //          it writes zeros for the sentinel rows and never reads them.
-//   wgrad  dB[e, n, c] = sum over expert e's rows of dC[p, n] A[p, c]: dC and A
-//          are transposed so that each expert's rows run along the contraction
-//          dimension from a 64-aligned start, zero-padded to whole 64-element
-//          k-blocks; then the grouped GEMM's weight-gradient kernel walks each
-//          expert's own k-blocks on CTA pairs (tcgen05 cta_group::2, the
-//          transposed A as the MMA's 256 rows and the transposed dC's rows as
-//          its columns, TMEM accumulators, TMA).
-// The padded layout is computed on the device from offsets: no host
-// synchronisation.
+//   wgrad  dB[e, n, c] = sum over expert e's rows of dC[p, n] A[p, c]: the
+//          grouped GEMM's weight-gradient kernel reads dC and A in place as
+//          MN-major operands (tcgen05 cta_group::2, A's features as the MMA's
+//          256 rows and dC's as its columns, TMEM accumulators, TMA), 64 rows
+//          of the expert per k-block; the expert's last, partial k-block comes
+//          from a zero-padded copy of its cnt mod 64 last rows (the tails), so
+//          no k-block reaches into the next expert's rows.
+// Both run on the device from offsets: no host synchronisation.
 #include <climits>
 
 #include "common.cuh"
@@ -22,119 +21,42 @@
 
 namespace {
 
-constexpr int kTile = 64;      // elements per side of a transposed tile
-constexpr int kPitch = 66;     // shared-memory row pitch in elements (33 words: fewer bank conflicts)
-constexpr int kColTiles = 8;   // column tiles per CTA of the padded transpose
 constexpr int kMaxE = 256;
+constexpr int kTailCols = 512;   // columns per CTA of the tail copy
 
-// One 64 x 64 bf16 tile: rows src_row(r) of src (or zeros), columns
-// [c0, c0 + 64) (C a multiple of 8), into dst[c0 + i][q0 + r].  16-byte global
-// loads and stores; the tile passes through shared memory as 4-byte words.
-template <class SrcRow>
-__device__ __forceinline__ void transpose_tile(const uint16_t* __restrict__ src, int64_t src_pitch, int C,
-                                               SrcRow src_row, uint16_t* __restrict__ dst, int64_t dst_pitch,
-                                               int64_t q0, int64_t q_end, int c0, uint16_t (*tile)[kPitch]) {
-    const int t = threadIdx.x;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {            // 64 rows x 8 vectors
-        const int idx = t + 256 * i, r = idx >> 3, v = idx & 7;
-        const int c = c0 + 8 * v;
-        const int64_t row = src_row(r);
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (row >= 0 && c < C) x = *reinterpret_cast<const uint4*>(src + row * src_pitch + c);
-        uint32_t* w = reinterpret_cast<uint32_t*>(&tile[r][8 * v]);
-        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {            // 64 output rows x 8 vectors
-        const int idx = t + 256 * i, cc = idx >> 3, v = idx & 7;
-        const int c = c0 + cc;
-        const int64_t q = q0 + 8 * v;
-        if (c < C && q < q_end) {
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                o[j] = static_cast<uint32_t>(tile[8 * v + 2 * j][cc]) |
-                       (static_cast<uint32_t>(tile[8 * v + 2 * j + 1][cc]) << 16);
-            *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(c) * dst_pitch + q) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
-    __syncthreads();
-}
-
-// Xt[c, q] for q in [0, P): the row of X that expert e's padded run puts at q,
-// or zero.  Expert e's run starts at poff[e] = 64 * sum_{e' < e} ceil(cnt_e'/64)
-// and holds its cnt_e rows (offsets[e] ..) followed by zeros.  A CTA resolves
-// its 64 columns q to source rows once, then transposes kColTiles tiles.
+// The tails of the weight gradient: for expert e with r = cnt_e mod 64 > 0,
+// rows [offsets[e + 1] - r, offsets[e + 1]) of X [M_cap, C] go to rows
+// [64e, 64e + r) of tail [64E, C] and rows [64e + r, 64e + 64) are zeroed.
+// blockIdx.z picks the operand (0: dC, 1: A); a CTA copies kTailCols columns
+// of one expert with 16-byte loads and stores.  Offsets that are not a
+// monotone prefix within M_cap are reported and no row is read.
 __global__ void __launch_bounds__(256)
-pad_transpose_kernel(const uint16_t* __restrict__ X, int C, const int32_t* __restrict__ offsets, int E,
-                     int M_cap, int64_t P, uint16_t* __restrict__ Xt, int* err) {
-    __shared__ int poff[kMaxE + 1];
-    __shared__ int bad;
-    __shared__ int64_t srow[kTile];
-    __shared__ __align__(16) uint16_t tile[kTile][kPitch];
-    const int tx = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (warp == 0) {   // check offsets; prefix of the padded counts, 8 experts per lane
-        int v[8], sum = 0, b = tx == 0 && (offsets[0] != 0 || offsets[E] > M_cap);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tx * 8 + i;
-            v[i] = 0;
-            if (e < E) {
-                const int cnt = offsets[e + 1] - offsets[e];
-                if (cnt < 0) b = 1;
-                v[i] = cnt > 0 ? (cnt + 63) / 64 * 64 : 0;
-            }
-            sum += v[i];
-        }
-        b = __any_sync(0xffffffffu, b);
-        if (tx == 0) bad = b;
-        int incl = sum;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (tx >= off) incl += o;
-        }
-        int run = incl - sum;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tx * 8 + i;
-            if (e < E) { poff[e] = run; run += v[i]; }
-        }
-        if (tx == 31) poff[E] = incl;
-    }
-    __syncthreads();
-    if (bad || poff[E] > P) {   // offsets that are not a monotone prefix within M_cap: nothing is read
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) moe::raise_device_error(err, MOE_DEVERR_OFFSETS);
+wgrad_tail_kernel(const uint16_t* __restrict__ dC, int N, const uint16_t* __restrict__ A, int K,
+                  const int32_t* __restrict__ offsets, int E, int M_cap, uint16_t* __restrict__ tails, int* err) {
+    const int e = blockIdx.x;
+    const uint16_t* X = blockIdx.z == 0 ? dC : A;
+    const int C = blockIdx.z == 0 ? N : K;
+    uint16_t* tail = tails + (blockIdx.z == 0 ? 0 : static_cast<int64_t>(64) * E * N);
+    const int c0 = blockIdx.y * kTailCols;
+    if (c0 >= C) return;
+    int bad = 0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= offsets[i + 1] < offsets[i];
+    if (threadIdx.x == 0) bad |= offsets[0] != 0 || offsets[E] > M_cap;
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) moe::raise_device_error(err, MOE_DEVERR_OFFSETS);
         return;
     }
-    const int64_t q0 = static_cast<int64_t>(blockIdx.x) * kTile;
-    if (threadIdx.x < kTile) {
-        const int64_t q = q0 + threadIdx.x;
-        int64_t row = -1;
-        if (q < poff[E]) {
-            int lo = 0, hi = E;   // largest e with poff[e] <= q
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (poff[mid] <= q) lo = mid; else hi = mid;
-            }
-            const int64_t j = q - poff[lo];
-            if (j < offsets[lo + 1] - offsets[lo]) row = offsets[lo] + j;
-        }
-        srow[threadIdx.x] = row;
+    const int lo = offsets[e], hi = offsets[e + 1];
+    const int r = (hi - lo) % 64;
+    if (r == 0) return;   // every k-block of this expert is read in place
+    constexpr int kVecs = kTailCols / 8;   // 16-byte vectors per row
+    for (int i = threadIdx.x; i < 64 * kVecs; i += blockDim.x) {
+        const int j = i / kVecs, c = c0 + 8 * (i % kVecs);
+        if (c >= C) continue;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (j < r) v = *reinterpret_cast<const uint4*>(X + static_cast<int64_t>(hi - r + j) * C + c);
+        *reinterpret_cast<uint4*>(tail + (static_cast<int64_t>(e) * 64 + j) * C + c) = v;
     }
-    __syncthreads();
-    for (int ct = 0; ct < kColTiles; ++ct) {
-        const int c0 = (blockIdx.y * kColTiles + ct) * kTile;
-        if (c0 >= C) break;
-        transpose_tile(X, C, C, [&](int r) { return srow[r]; }, Xt, P, q0, P, c0, tile);
-    }
-}
-
-// Columns of the padded layout: enough for any offsets with offsets[E] <= M_cap.
-int64_t padded_cols(int E, int M_cap) {
-    return (static_cast<int64_t>(M_cap) + 63) / 64 * 64 + static_cast<int64_t>(E) * 64;
 }
 
 }  // namespace
@@ -156,7 +78,7 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const void* dC, const void* B, co
 
 extern "C" size_t moe_grouped_gemm_wgrad_workspace_size(int E, int M_cap, int N, int K) {
     if (E < 1 || E > kMaxE || M_cap < 1 || N < 8 || K < 8) return 0;
-    return static_cast<size_t>(N + K) * static_cast<size_t>(padded_cols(E, M_cap)) * 2;
+    return static_cast<size_t>(N + K) * 64 * static_cast<size_t>(E) * 2;   // the tails
 }
 
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const void* A, const void* dC, const int32_t* offsets, int E,
@@ -171,17 +93,10 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const void* A, const void* dC, co
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t P = padded_cols(E, M_cap);
-    MOE_CHECK_ARG(P < INT_MAX);
-    uint16_t* dCt = static_cast<uint16_t*>(ws);             // [N, P]
-    uint16_t* At = dCt + static_cast<int64_t>(N) * P;       // [K, P]
-    const int64_t qb = P / kTile;   // P is a multiple of 64
-    const int span = kTile * kColTiles;
-    pad_transpose_kernel<<<dim3(static_cast<unsigned>(qb), (N + span - 1) / span), 256, 0, s>>>(
-        static_cast<const uint16_t*>(dC), N, offsets, E, M_cap, P, dCt, err);
+    const int span = (N > K ? N : K);
+    wgrad_tail_kernel<<<dim3(static_cast<unsigned>(E), (span + kTailCols - 1) / kTailCols, 2), 256, 0, s>>>(
+        static_cast<const uint16_t*>(dC), N, static_cast<const uint16_t*>(A), K, offsets, E, M_cap,
+        static_cast<uint16_t*>(ws), err);
     MOE_CHECK_LAUNCH();
-    pad_transpose_kernel<<<dim3(static_cast<unsigned>(qb), (K + span - 1) / span), 256, 0, s>>>(
-        static_cast<const uint16_t*>(A), K, offsets, E, M_cap, P, At, err);
-    MOE_CHECK_LAUNCH();
-    return moe::wgrad_gemm(dCt, At, P, offsets, E, M_cap, N, K, dB, s);
+    return moe::wgrad_gemm(dC, A, ws, offsets, E, M_cap, N, K, dB, s);
 }

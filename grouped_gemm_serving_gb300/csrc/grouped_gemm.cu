@@ -127,11 +127,11 @@ struct Params {
     const uint8_t* gx;
     const int32_t* sorted_rows;
     int T, topk;
-    // weight-gradient kernel (WG: pair, bf16 store): the "weights" are
-    // [out_cols, P] and the "tokens" [wg_rows, P], both with each expert's
-    // rows laid out along P from a 64-aligned start, zero-padded; every
-    // expert has all wg_rows x out_cols output tiles over its own k-blocks;
-    // the output is [E, wg_rows, out_cols].
+    // weight-gradient kernel (WG: pair, bf16 store): the "weights" are A
+    // [M_cap, out_cols] and the "tokens" dC [M_cap, wg_rows], both read
+    // MN-major over the expert's own rows; every expert has all
+    // wg_rows x out_cols output tiles over its own k-blocks; the output is
+    // [E, wg_rows, out_cols].
     int wg_rows;
     // swapped store tiles only: the weights are MN-major, B [E, K, N] with
     // the N output features contiguous (the data gradient reads the forward
@@ -187,15 +187,20 @@ static_assert(smem_bytes<false, EPI_STORE>() <= 227 * 1024 && smem_bytes<false, 
 // Tensor maps over the token operand of the swapped kernels with boxes of
 // 8, 16, .., 128 rows: a CTA's half of a token tile is one box of exactly
 // its height.
+// The weight gradient puts its four operand maps in the first slots instead:
+// A and dC in place, then their zero-padded tails (64 features x 64 rows
+// boxes, MN-major).
 constexpr int kTokenMaps = 16;
 struct TokenMaps {
     CUtensorMap m[kTokenMaps];
 };
+constexpr int kWgA = 0, kWgC = 1, kWgTailA = 2, kWgTailC = 3, kWgMaps = 4;
 
 struct Tile {
     int e, row0, row_end, col0;
     int rows;  // swapped: token rows of this tile (<= BT)
-    int kb0, nkb;  // the tile's k-blocks: [kb0, kb0 + nkb)
+    int nkb;    // the tile's k-blocks
+    int first;  // weight gradient: the expert's first row
 };
 
 // Weight gradient: every expert has the same wg_pair_mt(p) token tiles.
@@ -222,15 +227,16 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
     Tile ti;
     ti.e = lo;
     ti.row_end = p.offsets[lo + 1];
-    ti.kb0 = 0;
+    ti.first = 0;
     ti.nkb = p.k_blocks;
     if (WG) {
         // weight gradient on a pair: the tokens are the wg_rows output rows
-        // in tiles of BT, the K range the expert's zero-padded k-blocks
+        // in tiles of BT; the contraction runs over the expert's own rows in
+        // k-blocks of 64 (S.prefix is the k-block prefix)
         ti.row0 = (local % mt) * BT;
         ti.rows = min(BT, p.wg_rows - ti.row0);
         ti.row_end = p.wg_rows;
-        ti.kb0 = S.prefix[lo];
+        ti.first = p.offsets[lo];
         ti.nkb = S.prefix[lo + 1] - S.prefix[lo];
     } else if (SWAP) {
         // an expert's tokens in mt tiles of equal size (a multiple of 16),
@@ -383,9 +389,11 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
         const Tile ti = decode_tile<true, WG>(t, S, p);
         const int nh = swap_n(ti) / 2;                 // token rows in each CTA: 8 .. 128
         const CUtensorMap* tmXh = &tmX->m[nh / 8 - 1];
-        const int xbytes = nh * 128;
         const int xrow = ti.row0 + static_cast<int>(rank) * nh;
-        const int nkb = WG ? ti.nkb : p.k_blocks, kb0 = WG ? ti.kb0 : 0;
+        // weight gradient: this CTA's nh columns of dC in one or two 64-wide boxes
+        const int xbytes = WG ? (nh > 64 ? 2 : 1) * 8192 : nh * 128;
+        const int nkb = WG ? ti.nkb : p.k_blocks;
+        const int nfull = WG ? (p.offsets[ti.e + 1] - ti.first) / 64 : 0;   // k-blocks read in place
         for (int kb = 0; kb < nkb; ++kb) {
             const bool got = moe::mbar_wait(bar(S.empty[stage]), phase ^ 1u, &S.abort_flag, kWaitNs);
             if (!__all_sync(0xffffffffu, got)) {
@@ -395,12 +403,23 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
             const uint32_t fb = moe::map_to_cta(bar(S.full[stage]), 0);
             const uint32_t sa = moe::smem_u32(stages + stage * Geo<true, EPI>::kStageBytes);
             const uint32_t sb = sa + kStageA;
-            const int kc = (kb0 + kb) * 64;
+            const int kc = kb * 64;
             if (moe::elect_one()) {
                 if (rank == 0) moe::mbar_arrive_expect_tx(bar(S.full[stage]), 2 * (kStageA + xbytes));
                 if (WG) {
-                    // weight gradient: the "weights" are the transposed [out_cols, P] operand
-                    moe::tma_load_2d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128);
+                    // weight gradient: A's 128 features and dC's nh columns of
+                    // this CTA over 64 rows, as 64 x 64 MN-major swizzle atoms
+                    // 8 KB apart, from the expert's own rows or, for its
+                    // partial last k-block, from the zero-padded tails
+                    const bool in_place = kb < nfull;
+                    const CUtensorMap* ma = &tmX->m[in_place ? kWgA : kWgTailA];
+                    const CUtensorMap* mc = &tmX->m[in_place ? kWgC : kWgTailC];
+                    const int row = in_place ? ti.first + kc : ti.e * 64;
+                    const int f0 = ti.col0 + static_cast<int>(rank) * 128;
+                    moe::tma_load_2d_pair(sa, ma, fb, f0, row);
+                    moe::tma_load_2d_pair(sa + 8192, ma, fb, f0 + 64, row);
+                    moe::tma_load_2d_pair(sb, mc, fb, xrow, row);
+                    if (nh > 64) moe::tma_load_2d_pair(sb + 8192, mc, fb, xrow + 64, row);
                 } else if (EPI == EPI_STORE && p.mn_a) {
                     // two 64-feature x 64-row swizzle atoms, 8 KB apart
                     const int f0 = ti.col0 + static_cast<int>(rank) * 128;
@@ -410,7 +429,7 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
                     moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
                 else   // 8 groups of (8 gate rows, 8 up rows) of this CTA's 64 features
                     moe::tma_load_5d_pair(sa, tmW, fb, kc, 0, 0, (ti.col0 + static_cast<int>(rank) * 64) / 8, ti.e);
-                moe::tma_load_2d_pair(sb, tmXh, fb, kc, xrow);
+                if (!WG) moe::tma_load_2d_pair(sb, tmXh, fb, kc, xrow);
             }
             __syncwarp();
             issued |= 1u << stage;
@@ -542,7 +561,8 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
     for (int t = tile_first<SWAP>(); ok && t < total; t += tile_step<SWAP>()) {
         if (SWAP) {
             const int n = swap_n(decode_tile<true, WG>(t, S, p));
-            idesc = EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n) : moe::make_idesc(1u, 2 * BM, n);
+            idesc = WG ? moe::make_idesc_ab_mn(1u, 2 * BM, n)
+                 : EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n) : moe::make_idesc(1u, 2 * BM, n);
         }
         if (!FP8) {
             // with a pair, the peer's epilogue arrives here from the other CTA
@@ -564,12 +584,14 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             moe::tc_fence_after();
             const uint32_t sa = moe::smem_u32(stages + stage * Geo<SWAP, EPI>::kStageBytes);
-            // MN-major weights (swapped store tiles of the data gradient): a K
-            // step of 16 rows is 2 KB further on; K-major: 32 bytes
-            const bool amn = SWAP && EPI == EPI_STORE && p.mn_a;
+            // MN-major operands (the data gradient's weights; both operands of
+            // the weight gradient): a K step of 16 rows is 2 KB further on;
+            // K-major: 32 bytes
+            const bool amn = WG || (SWAP && EPI == EPI_STORE && p.mn_a);
             const uint64_t adesc = amn ? moe::smem_desc_sw128_mn(sa, 8192) : moe::smem_desc_sw128(sa);
             const uint64_t astep = amn ? 2048 >> 4 : 2;
-            const uint64_t bdesc = moe::smem_desc_sw128(sa + kStageA);
+            const uint64_t bdesc = WG ? moe::smem_desc_sw128_mn(sa + kStageA, 8192) : moe::smem_desc_sw128(sa + kStageA);
+            const uint64_t bstep = WG ? 2048 >> 4 : 2;
             const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
             // the same (lowest) lane is elected every time, so its commits
             // track all the MMAs it issued
@@ -579,7 +601,7 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
                     if (FP8)
                         moe::mma_fp8(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0);
                     else if (SWAP)
-                        moe::mma_bf16_pair(d, adesc + astep * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                        moe::mma_bf16_pair(d, adesc + astep * k, bdesc + bstep * k, idesc, (kb | k) != 0);
                     else
                         moe::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
                 if (SWAP) moe::tc_commit_pair(bar(S.empty[stage]), 0x3);   // frees the stage in both CTAs
@@ -1101,7 +1123,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         moe::prefetch_tensormap(&tmA);
         moe::prefetch_tensormap(&tmB);
         if (SWAP) {
-            for (int j = 0; j < kTokenMaps; ++j) moe::prefetch_tensormap(&tmX.m[j]);
+            for (int j = 0; j < (WG ? kWgMaps : kTokenMaps); ++j) moe::prefetch_tensormap(&tmX.m[j]);
         }
     }
     __syncthreads();
@@ -1389,31 +1411,32 @@ moe_status_t moe::dgrad_gemm(const void* dC, const void* B, const int32_t* offse
                             MOE_EPI_STORE, dA, nullptr, reinterpret_cast<moe_stream_t>(s), true);
 }
 
-moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, const int32_t* offsets, int E,
+moe_status_t moe::wgrad_gemm(const void* dC, const void* A, const void* tails, const int32_t* offsets, int E,
                              int M_cap, int N, int K, void* dB, cudaStream_t s) {
-    // dB[e] [N, K] = At_g[:, run_e] x Bt_g[:, run_e]^T over expert e's padded
-    // run of P.  Swapped operands on CTA pairs: Bt_g [K, P] supplies the
-    // MMA's M rows (the output features, 256 per pair tile), At_g [N, P] its
-    // N columns (the output rows, in tiles of up to 256).
-    MOE_CHECK_ARG(At_g && Bt_g && offsets && dB && E >= 1 && E <= kMaxE && M_cap >= 1);
-    MOE_CHECK_ARG(N >= 8 && N % 8 == 0 && K >= 8 && K % 8 == 0 && P >= 64 && P % 64 == 0);
-    MOE_CHECK_ARG(P < INT_MAX && static_cast<int64_t>(E) * N < INT_MAX);
+    // dB[e] [N, K] = dC_e^T A_e over expert e's rows.  Swapped operands on CTA
+    // pairs: A supplies the MMA's M rows (the output features, 256 per pair
+    // tile), dC its N columns (the output rows, in tiles of up to 256); both
+    // are read MN-major, 64 features x 64 rows per box, from their own rows or,
+    // for an expert's partial last k-block, from the zero-padded tails.
+    MOE_CHECK_ARG(dC && A && tails && offsets && dB && E >= 1 && E <= kMaxE && M_cap >= 1);
+    MOE_CHECK_ARG(N >= 8 && N % 8 == 0 && K >= 8 && K % 8 == 0);
+    MOE_CHECK_ARG(moe::aligned16(dC) && moe::aligned16(A) && moe::aligned16(tails) && moe::aligned16(dB));
+    MOE_CHECK_ARG(static_cast<int64_t>(E) * N < INT_MAX);
     const int n_tiles = (K + kSwapFeatStore - 1) / kSwapFeatStore;
     MOE_CHECK_ARG(static_cast<int64_t>(E) * ((N + BT - 1) / BT) * n_tiles < INT_MAX);
     int* err = moe::device_error_word();
     if (!err) return MOE_ERR_CUDA;
-    CUtensorMap tmW;
     TokenMaps tmX{};
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(K)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
-        const cuuint32_t box[2] = {64, 128};   // 128 output features per CTA
-        if (!encode(&tmW, false, Bt_g, 2, dims, strides, box)) return MOE_ERR_CUDA;
-    }
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
-        if (!encode_token_maps(&tmX, At_g, dims, strides)) return MOE_ERR_CUDA;
+    const cuuint32_t box[2] = {64, 64};
+    const uint8_t* tail_c = static_cast<const uint8_t*>(tails);
+    const uint8_t* tail_a = tail_c + static_cast<size_t>(64) * E * N * 2;
+    const struct { const void* base; int cols; cuuint64_t rows; } ops[4] = {
+        {A, K, static_cast<cuuint64_t>(M_cap)}, {dC, N, static_cast<cuuint64_t>(M_cap)},
+        {tail_a, K, static_cast<cuuint64_t>(64) * E}, {tail_c, N, static_cast<cuuint64_t>(64) * E}};
+    for (int i = 0; i < kWgMaps; ++i) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(ops[i].cols), ops[i].rows};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ops[i].cols) * 2};
+        if (!encode(&tmX.m[i], false, ops[i].base, 2, dims, strides, box)) return MOE_ERR_CUDA;
     }
     Params p{};
     p.offsets = offsets;
@@ -1430,7 +1453,7 @@ moe_status_t moe::wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, cons
     p.nb_scale = 0;
     p.topk = 1;
     p.wg_rows = N;
-    return launch<false, EPI_STORE, true, true>(tmX.m[kTokenMaps - 1], tmW, tmX, p, s);
+    return launch<false, EPI_STORE, true, true>(tmX.m[kWgA], tmX.m[kWgC], tmX, p, s);
 }
 
 extern "C" moe_status_t moe_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_scales,

@@ -13,12 +13,14 @@ moe_status_t dgrad_gemm(const void* dC, const void* B, const int32_t* offsets, i
                         void* dA, cudaStream_t stream);
 
 // Launches the grouped GEMM's weight-gradient kernel on CTA pairs (grouped_gemm.cu):
-//   dB[e, n, c] = sum_j At_g[n, P_e + j] * Bt_g[c, P_e + j]
-// over expert e's zero-padded run [P_e, P_e + 64 * ceil(cnt_e / 64)) of the
-// transposed operands At_g bf16 [N, P] and Bt_g bf16 [K, P] (P a multiple of
-// 64), where cnt_e = offsets[e + 1] - offsets[e] and P_e the prefix of the
-// padded counts.  dB bf16 [E, N, K]; an expert without rows gets zeros.
-moe_status_t wgrad_gemm(const void* At_g, const void* Bt_g, int64_t P, const int32_t* offsets, int E,
+//   dB[e, n, c] = sum over expert e's rows p of dC[p, n] * A[p, c]
+// with dC bf16 [M_cap, N] and A bf16 [M_cap, K] read in place (MN-major), in
+// 64-row k-blocks from offsets[e].  An expert's last, partial k-block
+// (cnt_e mod 64 rows, cnt_e = offsets[e + 1] - offsets[e]) comes instead from
+// rows [64e, 64e + 64) of the tails, zero-padded copies of those rows:
+// dC's bf16 [64E, N] followed by A's bf16 [64E, K].  dB bf16 [E, N, K]; an
+// expert without rows gets zeros.
+moe_status_t wgrad_gemm(const void* dC, const void* A, const void* tails, const int32_t* offsets, int E,
                         int M_cap, int N, int K, void* dB, cudaStream_t stream);
 
 }  // namespace moe

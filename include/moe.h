@@ -346,8 +346,9 @@ moe_status_t moe_grouped_gemm_combine(const void* h, const void* W2, const int32
  *   offsets[e+1]) of dC[p, n] * A[p, c]; an expert without rows gets zeros;
  *   rows p >= offsets[E] of A and dC are never read.
  *   A bf16 [M_cap, K]; dC bf16 [M_cap, N]; dB bf16 [E, N, K].
- *   Workspace: moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K) bytes
- *   (dC and A transposed, each expert's rows zero-padded to a multiple of 64).
+ *   A and dC are read in place.  Workspace:
+ *   moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K) bytes, 128 (N + K) E:
+ *   each expert's last cnt mod 64 rows of dC and A, zero-padded to 64 rows.
  * Limits: 1 <= E <= 256, N and K positive multiples of 8; offsets not a
  *   monotone prefix from 0 to at most M_cap: MOE_DEVERR_OFFSETS, nothing
  *   computed.  Missing or small workspace: MOE_ERR_WORKSPACE.

@@ -2,7 +2,8 @@
 moe_grouped_gemm_wgrad) against the CPU oracle.
 
 Shapes span several tiles with ragged tails: experts of 0, a few and several
-hundred rows (the wgrad k-blocks are each expert's own zero-padded run), N
+hundred rows (wgrad reads each expert's rows in 64-row k-blocks, its partial
+last block from a zero-padded copy: remainders 0, 1, 31, 32, 33 and 63), N
 and K not multiples of the tile.  Sentinel rows of the inputs are NaN: dA's
 sentinel rows must come out exactly zero and nothing else may change.  The
 full-size case (the 32-expert layer's gate_up shape) is checked on sampled
