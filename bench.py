@@ -663,10 +663,14 @@ def grad_main(args, wl, synth, torch, moe):
         "down wgrad": lambda: moe.moe_grouped_gemm_wgrad(h, dY2, off, E, R, H, I, dW2, ws, ws_n),
     }
     flop = {"gate_up": 2.0 * live * 2 * I * H, "down": 2.0 * live * H * I}
+    # wgrad writes the whole dB (E * N * K bf16): a second bound besides the
+    # tensor pipe, against the write-only bandwidth measured here as a memset
+    # of the gate_up dB buffer, timed like the ops
+    out_bytes = {"gate_up": dW1.numel() * 2, "down": dW2.numel() * 2}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    rows = []
-    for name, f in ops.items():
+
+    def timed(f):
         for _ in range(max(3, args.warmup)):
             f()
         torch.cuda.synchronize()
@@ -678,9 +682,18 @@ def grad_main(args, wl, synth, torch, moe):
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
-        ms = statistics.fmean(ts)
+        return statistics.fmean(ts)
+
+    write_gbs = out_bytes["gate_up"] / (timed(lambda: dW1.zero_()) * 1e-3) / 1e9
+    rows = []
+    for name, f in ops.items():
+        ms = timed(f)
         tf = flop[name.split()[0]] / (ms * 1e-3) / 1e12
-        rows.append({"op": name, "ms": ms, "tflops": tf, "frac": tf / pk["bf16_tflops"]})
+        row = {"op": name, "ms": ms, "tflops": tf, "frac": tf / pk["bf16_tflops"]}
+        if name.endswith("wgrad"):
+            wgbs = out_bytes[name.split()[0]] / (ms * 1e-3) / 1e9
+            row.update({"out_bytes": out_bytes[name.split()[0]], "write_gbs": wgbs, "write_frac": wgbs / write_gbs})
+        rows.append(row)
     if moe.moe_get_device_error() != 0:
         raise SystemExit("device error in the gradient bench")
     print(json.dumps({"metric": "grouped GEMM forward and gradients", "unit": "TFLOP/s",
@@ -688,7 +701,9 @@ def grad_main(args, wl, synth, torch, moe):
                                  "steps": args.steps, "note": "dgrad reads the weights in place; wgrad reads the "
                                  "activations and output gradients in place and includes the copy of "
                                  "each expert's partial last 64 rows"},
-                      "peak": {"bf16_tflops": pk["bf16_tflops"], "kind": pk_kind}, "rows": rows}))
+                      "peak": {"bf16_tflops": pk["bf16_tflops"], "kind": pk_kind,
+                               "write_gbs": write_gbs, "write_kind": "memset of the gate_up dB buffer, measured here"},
+                      "rows": rows}))
     return 0
 
 
