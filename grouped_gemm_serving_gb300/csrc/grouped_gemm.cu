@@ -25,7 +25,11 @@
 // interleaved in groups of 8 (8 gate rows, the same 8 up rows, ...), so a
 // feature's gate and up accumulators sit 8 lanes apart in one warp: the two
 // lanes swap half of each 32-token chunk with one shuffle per token and
-// both compute silu(g) * u.
+// both compute silu(g) * u.  An expert's last SwiGLU tile, when at most 64 of
+// its 128 features exist (I = 2880: 2880 = 22.5 x 128), is an M = 128 pair
+// MMA instead (N rounded up to 32): each CTA stages 64 weight rows (32
+// features) and its accumulator holds weight row l % 64 for tokens
+// (l / 64) * N/2 + column in lane l, columns below N/2.
 //
 // FP8 (and gathered A): single CTAs, 128 rows (tokens) x 256 columns
 // (weights), 48 KB per k-block, four deep.  Each 128-wide k-block is an exact
@@ -199,6 +203,10 @@ constexpr int kWgA = 0, kWgC = 1, kWgTailA = 2, kWgTailC = 3, kWgMaps = 4;
 struct Tile {
     int e, row0, row_end, col0;
     int rows;  // swapped: token rows of this tile (<= BT)
+    // swapped SwiGLU: the expert's last feature tile, at most half used
+    // (<= 64 h features), runs as an M = 128 pair MMA (each CTA: 32
+    // features' 64 gate and up rows)
+    bool half;
     int nkb;    // the tile's k-blocks
     int first;  // weight gradient: the expert's first row
 };
@@ -229,6 +237,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
     ti.row_end = p.offsets[lo + 1];
     ti.first = 0;
     ti.nkb = p.k_blocks;
+    ti.half = false;
     if (WG) {
         // weight gradient on a pair: the tokens are the wg_rows output rows
         // in tiles of BT; the contraction runs over the expert's own rows in
@@ -251,6 +260,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
         ti.rows = 0;
     }
     ti.col0 = (local / mt) * (SWAP ? (p.half ? kSwapFeatSwiglu : kSwapFeatStore) : (p.half ? BN / 2 : BN));
+    if (SWAP && !WG && p.half) ti.half = p.half - ti.col0 <= kSwapFeatSwiglu / 2;
     return ti;
 }
 
@@ -363,7 +373,8 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
 // Token rows of a swapped tile (at most BT; the MMA's N is this rounded up to 16,
 // which cta_group::2 M = 256 MMAs allow).
 __device__ __forceinline__ int swap_rows(const Tile& ti) { return ti.rows; }
-__device__ __forceinline__ int swap_n(const Tile& ti) { return (ti.rows + 15) & ~15; }
+// MMA N of a swapped tile: the tokens rounded up to 16 (M = 256) or 32 (M = 128)
+__device__ __forceinline__ int swap_n(const Tile& ti) { return ti.half ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15; }
 
 // Tile loop bounds: a CTA pair walks the tile list as one unit.
 template <bool PAIR>
@@ -375,12 +386,13 @@ __device__ __forceinline__ int tile_step() { return PAIR ? gridDim.x >> 1 : grid
 // loads its 128 weight rows into the A region and its N/2 token rows into
 // the B region, all counted on the leading CTA's full barrier (the leader
 // posts both CTAs' bytes).  SwiGLU: CTA r's 128 weight rows are its 64
-// features' gate and up rows, interleaved in groups of 8 (one 5-D box).
+// features' gate and up rows, interleaved in groups of 8 (one 5-D box; an
+// M = 128 tile takes 4 groups, 32 features, from tmW64).
 // Tokens: one box of exactly the tile's N/2 rows (a multiple of 8, one
 // tensor map per height).  A TMA instruction costs the issuing thread many
 // cycles, so a k-block takes as few as possible.
 template <int EPI, bool WG>
-__device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
+__device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW, const CUtensorMap* tmW64,
                               uint8_t* stages, Shared& S, const Params& p, int total, uint32_t rank) {
     int stage = 0;
     uint32_t phase = 0, issued = 0, issued_par = 0;
@@ -392,6 +404,7 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
         const int xrow = ti.row0 + static_cast<int>(rank) * nh;
         // weight gradient: this CTA's nh columns of dC in one or two 64-wide boxes
         const int xbytes = WG ? (nh > 64 ? 2 : 1) * 8192 : nh * 128;
+        const int abytes = ti.half ? kStageA / 2 : kStageA;   // M = 128: 64 weight rows per CTA (SwiGLU)
         const int nkb = WG ? ti.nkb : p.k_blocks;
         const int nfull = WG ? (p.offsets[ti.e + 1] - ti.first) / 64 : 0;   // k-blocks read in place
         for (int kb = 0; kb < nkb; ++kb) {
@@ -405,7 +418,7 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
             const uint32_t sb = sa + kStageA;
             const int kc = kb * 64;
             if (moe::elect_one()) {
-                if (rank == 0) moe::mbar_arrive_expect_tx(bar(S.full[stage]), 2 * (kStageA + xbytes));
+                if (rank == 0) moe::mbar_arrive_expect_tx(bar(S.full[stage]), 2 * (abytes + xbytes));
                 if (WG) {
                     // weight gradient: A's 128 features and dC's nh columns of
                     // this CTA over 64 rows, as 64 x 64 MN-major swizzle atoms
@@ -425,10 +438,13 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW,
                     const int f0 = ti.col0 + static_cast<int>(rank) * 128;
                     moe::tma_load_3d_pair(sa, tmW, fb, f0, kc, ti.e);
                     moe::tma_load_3d_pair(sa + 8192, tmW, fb, f0 + 64, kc, ti.e);
-                } else if (EPI == EPI_STORE)
+                } else if (EPI == EPI_STORE) {
                     moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
-                else   // 8 groups of (8 gate rows, 8 up rows) of this CTA's 64 features
+                } else if (ti.half) {   // 4 groups: this CTA's 32 features
+                    moe::tma_load_5d_pair(sa, tmW64, fb, kc, 0, 0, (ti.col0 + static_cast<int>(rank) * 32) / 8, ti.e);
+                } else {   // 8 groups of (8 gate rows, 8 up rows) of this CTA's 64 features
                     moe::tma_load_5d_pair(sa, tmW, fb, kc, 0, 0, (ti.col0 + static_cast<int>(rank) * 64) / 8, ti.e);
+                }
                 if (!WG) moe::tma_load_2d_pair(sb, tmXh, fb, kc, xrow);
             }
             __syncwarp();
@@ -560,9 +576,11 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
     bool ok = true, issued = false;
     for (int t = tile_first<SWAP>(); ok && t < total; t += tile_step<SWAP>()) {
         if (SWAP) {
-            const int n = swap_n(decode_tile<true, WG>(t, S, p));
+            const Tile ti = decode_tile<true, WG>(t, S, p);
+            const int n = swap_n(ti);
             idesc = WG ? moe::make_idesc_ab_mn(1u, 2 * BM, n)
-                 : EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n) : moe::make_idesc(1u, 2 * BM, n);
+                 : EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n)
+                 : moe::make_idesc(1u, ti.half ? BM : 2 * BM, n);
         }
         if (!FP8) {
             // with a pair, the peer's epilogue arrives here from the other CTA
@@ -761,6 +779,42 @@ __device__ void fused_combine_empty_tokens(const Params& p) {
     }
 }
 
+// SwiGLU M = 128 tile: lane l of this CTA holds weight row l % 64 (its 32
+// features' gate and up rows, interleaved in groups of 8 as in a full tile)
+// for token (l / 64) * nh + column, columns below nh = N/2.  Each half of the
+// epilogue takes 64 columns; gate and up lanes swap halves of each 32-column
+// chunk as in a full tile.
+__device__ __forceinline__ void swiglu_half_tile(const Params& p, const Tile& ti, uint32_t ta, int q, int hsel,
+                                                 int lane, uint32_t rank) {
+    const int nh = swap_n(ti) / 2, tok0 = (q >> 1) * nh, ntok = ti.rows;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+        const int col = hsel * 64 + c * 32;
+        if (col >= nh || tok0 + col >= ntok) break;   // the same for the whole warp
+        const int jmax = min(32, min(nh - col, ntok - tok0 - col));   // token columns of the chunk
+        uint32_t v[32];
+        moe::tmem_ld32(ta + col, v);
+        moe::tmem_ld_wait();
+        const int r = (lane >> 3) & 1;   // 0: gate lane, 1: up lane
+        float h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[16 + j]);
+            const float o = __shfl_xor_sync(0xffffffffu, r ? lo : hi, 8);
+            h[j] = r ? silu_mul(o, hi) : silu_mul(lo, o);
+        }
+        const int f = ti.col0 + static_cast<int>(rank) * 32 + 16 * (q & 1) + 8 * (lane >> 4) + (lane & 7);
+        const int t0 = 16 * r;   // within the chunk
+        if (f < p.out_cols) {
+            __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + tok0 + col + t0) * p.out_cols + f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (t0 + j < jmax) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(h[j]);
+        }
+    }
+}
+
 template <bool FP8, int EPI, bool SWAP, bool WG>
 __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -792,49 +846,53 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             // weight gradient: expert e's output rows start at e * wg_rows
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
                                  (WG ? static_cast<int64_t>(ti.e) * p.wg_rows * p.out_cols : 0);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const int col = hsel * 128 + c * 32;
-                if (col >= ntok) break;                       // the same for the whole warp
-                uint32_t v[32];
-                if (!WG || ti.nkb > 0) {
-                    moe::tmem_ld32(ta + col, v);
-                    moe::tmem_ld_wait();
-                } else {   // an expert without rows: its weight gradient is zero
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-                if (EPI == EPI_STORE) {
-                    // one output feature per lane; a warp store covers 64
-                    // contiguous bytes of one token row
-                    const int f = ti.col0 + static_cast<int>(rank) * 128 + q * 32 + lane;
-                    if (f < p.out_cols) {
-                        __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + col) * p.out_cols + f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            if (EPI != EPI_STORE && ti.half) {
+                swiglu_half_tile(p, ti, ta, q, hsel, lane, rank);
+            } else {
+    #pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    const int col = hsel * 128 + c * 32;
+                    if (col >= ntok) break;                       // the same for the whole warp
+                    uint32_t v[32];
+                    if (!WG || ti.nkb > 0) {
+                        moe::tmem_ld32(ta + col, v);
+                        moe::tmem_ld_wait();
+                    } else {   // an expert without rows: its weight gradient is zero
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
                     }
-                } else {
-                    // lane l holds the gate (up, if bit 3 of l is set) row of
-                    // feature 16q + 8(l / 16) + l % 8; lanes l and l ^ 8 share
-                    // a feature.  The gate lane computes the chunk's first 16
-                    // tokens, the up lane the last 16, each receiving the
-                    // other's values for its tokens.
-                    const int r = (lane >> 3) & 1;            // 0: gate lane, 1: up lane
-                    float h[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[16 + j]);
-                        const float o = __shfl_xor_sync(0xffffffffu, r ? lo : hi, 8);
-                        h[j] = r ? silu_mul(o, hi) : silu_mul(lo, o);
-                    }
-                    const int f = ti.col0 + static_cast<int>(rank) * 64 + 16 * q + 8 * (lane >> 4) + (lane & 7);
-                    const int t0 = col + 16 * r;
-                    if (f < p.out_cols) {
-                        __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + t0) * p.out_cols + f;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (t0 + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(h[j]);
+                    if (EPI == EPI_STORE) {
+                        // one output feature per lane; a warp store covers 64
+                        // contiguous bytes of one token row
+                        const int f = ti.col0 + static_cast<int>(rank) * 128 + q * 32 + lane;
+                        if (f < p.out_cols) {
+                            __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + col) * p.out_cols + f;
+    #pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (col + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                        }
+                    } else {
+                        // lane l holds the gate (up, if bit 3 of l is set) row of
+                        // feature 16q + 8(l / 16) + l % 8; lanes l and l ^ 8 share
+                        // a feature.  The gate lane computes the chunk's first 16
+                        // tokens, the up lane the last 16, each receiving the
+                        // other's values for its tokens.
+                        const int r = (lane >> 3) & 1;            // 0: gate lane, 1: up lane
+                        float h[16];
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[16 + j]);
+                            const float o = __shfl_xor_sync(0xffffffffu, r ? lo : hi, 8);
+                            h[j] = r ? silu_mul(o, hi) : silu_mul(lo, o);
+                        }
+                        const int f = ti.col0 + static_cast<int>(rank) * 64 + 16 * q + 8 * (lane >> 4) + (lane & 7);
+                        const int t0 = col + 16 * r;
+                        if (f < p.out_cols) {
+                            __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + t0) * p.out_cols + f;
+    #pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (t0 + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(h[j]);
+                        }
                     }
                 }
             }
@@ -1159,7 +1217,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             producer_gather<FP8, EPI>(&tmA, &tmB, stages, S, p, total, warp == 0 ? 0 : warp - 1);
             __syncwarp();
         } else if (warp == 0) {
-            if (SWAP) producer_swap<EPI, WG>(&tmX, &tmB, stages, S, p, total, rank);
+            if (SWAP) producer_swap<EPI, WG>(&tmX, &tmB, &tmA, stages, S, p, total, rank);
             else producer<FP8, EPI>(&tmA, &tmB, stages, S, p, total);
         } else if (warp == 1) {
             if (rank == 0) mma_issuer<FP8, EPI, SWAP, WG>(stages, S, p, total, tmem);
@@ -1314,8 +1372,8 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
         // 128 rows); gathered A: x [T, K] read a row at a time
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(gx ? T : M_cap)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * esz};
-        const cuuint32_t box[2] = {bk, gx ? 1u : swap ? static_cast<cuuint32_t>(BT) : static_cast<cuuint32_t>(BM)};
-        if (!encode(&tmA, fp8, A, 2, dims, strides, box)) return MOE_ERR_CUDA;
+        const cuuint32_t box[2] = {bk, gx ? 1u : static_cast<cuuint32_t>(BM)};
+        if (!swap && !encode(&tmA, fp8, A, 2, dims, strides, box)) return MOE_ERR_CUDA;
         if (swap && !encode_token_maps(&tmX, A, dims, strides)) return MOE_ERR_CUDA;
     }
     if (weights_mn) {
@@ -1325,11 +1383,13 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(K) * N * 2};
         const cuuint32_t box[3] = {64, 64, 1};
         if (!encode(&tmB, false, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
+        tmA = tmB;   // unused here; the kernel only prefetches it
     } else if (!swiglu) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(N) * K * esz};
         const cuuint32_t box[3] = {bk, swap ? 128u : BN, 1};   // swapped: 128 weight rows per CTA
         if (!encode(&tmB, fp8, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
+        if (swap) tmA = tmB;   // unused by the swapped store kernel; it only prefetches it
     } else if (swap) {
         // [E, N/2/8, 2, 8, K] in memory order (expert, group of 8 features,
         // gate/up, feature in group, k): one box holds 8 groups of 8 gate rows
@@ -1340,6 +1400,9 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
                                        static_cast<cuuint64_t>(8) * K * esz, static_cast<cuuint64_t>(N) * K * esz};
         const cuuint32_t box[5] = {bk, 8, 2, 8, 1};
         if (!encode(&tmB, fp8, B, 5, dims, strides, box)) return MOE_ERR_CUDA;
+        // tmA: 4 groups (32 features, 64 rows) per box, for the M = 128 tile
+        const cuuint32_t box4[5] = {bk, 8, 2, 4, 1};
+        if (!encode(&tmA, fp8, B, 5, dims, strides, box4)) return MOE_ERR_CUDA;
     } else {
         // [E, 2, N/2, K]: a gate box clips at N/2 instead of running into the up rows
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(half), 2,
