@@ -176,6 +176,30 @@ def test_bf16_token_tile_boundaries(moe, epi, counts):
     assert np.all(host_bf16_bits(C)[live:] == 0)
 
 
+# The last SwiGLU feature tile of an expert holds I mod 128 features; when
+# that is at most 64 it runs as an M = 128 pair MMA (its own accumulator
+# layout, N rounded up to 32).  I = 8 .. 192 puts 8, 40, 64, 8, 56 and 64
+# features there; I = 200 (72 features) is the M = 256 control.  Token counts
+# cross the 16- and 32-rounding of N.
+@pytest.mark.parametrize("counts", ["boundaries", "box_heights"])
+@pytest.mark.parametrize("I", [8, 40, 64, 136, 184, 192, 200])
+def test_bf16_swiglu_half_used_last_tile(moe, I, counts):
+    counts = PAIR_COUNTS if counts == "boundaries" else BOX_COUNTS
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap, K = live + 24, 128
+    A = synth.grouped_rows(M_cap, K, live, seed=I + 5)
+    B = _weights(E, 2 * I, K, 9)
+    ref = oracle.swiglu(oracle.grouped_gemm_bf16(A, B, off), live)
+    h = torch.full((M_cap, I), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, dev_bf16(A), None, dev_bf16(B), None, dev(off), E, M_cap, 2 * I, K,
+                         moe.MOE_EPI_SWIGLU, h, None)
+    assert moe.moe_get_device_error() == 0
+    assert_close_bf16(host_f32_from_bf16(h)[:live], ref[:live])
+    assert np.all(host_bf16_bits(h)[live:] == 0)
+
+
 # FP8 tiles an expert's rows 128 at a time.  Expert sizes around those
 # boundaries (and 15-17, 31-33 rows: warps whose 32 rows are partly or wholly
 # past the expert's end), for all three epilogues, with several column tiles.
