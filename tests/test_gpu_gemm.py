@@ -176,6 +176,30 @@ def test_bf16_token_tile_boundaries(moe, epi, counts):
     assert np.all(host_bf16_bits(C)[live:] == 0)
 
 
+@pytest.mark.parametrize("epi", ["store", "swiglu"])
+def test_bf16_256_experts(moe, epi):
+    # the most experts the library takes (the tile prefix holds 8 per lane),
+    # counts from 0 to 300 rows
+    E, K = 256, 64
+    counts = np.array([(37 * e) % 301 if e % 7 else 0 for e in range(E)], np.int64)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap = live + 8
+    N = 136 if epi == "store" else 2 * 72
+    A = synth.grouped_rows(M_cap, K, live, seed=256)
+    B = _weights(E, N, K, 11)
+    ref = oracle.grouped_gemm_bf16(A, B, off)
+    if epi == "swiglu":
+        ref = oracle.swiglu(ref, live)
+    ncol = N if epi == "store" else N // 2
+    C = torch.full((M_cap, ncol), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, dev_bf16(A), None, dev_bf16(B), None, dev(off), E, M_cap, N, K,
+                         moe.MOE_EPI_STORE if epi == "store" else moe.MOE_EPI_SWIGLU, C, None)
+    assert moe.moe_get_device_error() == 0
+    assert_close_bf16(host_f32_from_bf16(C)[:live], ref[:live])
+    assert np.all(host_bf16_bits(C)[live:] == 0)
+
+
 # The last SwiGLU feature tile of an expert holds I mod 128 features; when
 # that is at most 64 it runs as an M = 128 pair MMA (its own accumulator
 # layout, N rounded up to 32).  I = 8 .. 192 puts 8, 40, 64, 8, 56 and 64

@@ -86,6 +86,31 @@ def test_wgrad(moe, E, M_cap, live, N, K, counts):
             assert_close_bf16(got[e], ref[e])
 
 
+def test_wgrad_256_experts_every_tail(moe):
+    # the most experts the library takes: every remainder mod 64 (the tail copy)
+    # and empty experts, 8 experts per lane in the kernel's prefix
+    E, N, K = 256, 72, 40
+    counts = np.array([(7 * e) % 131 if e % 9 else 0 for e in range(E)], np.int64)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap = live + 16
+    A = synth.dense_rows(M_cap, K, seed=31, std=1.0, tensor_id=1)
+    dC = synth.dense_rows(M_cap, N, seed=32, std=1.0, tensor_id=2)
+    A[live:] = BF16_NAN
+    dC[live:] = BF16_NAN
+    ref = oracle.grouped_gemm_wgrad_bf16(A, dC, off, E)
+    dB = torch.full((E, N, K), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    n = moe.moe_grouped_gemm_wgrad_workspace_size(E, M_cap, N, K)
+    moe.moe_grouped_gemm_wgrad(dev_bf16(A), dev_bf16(dC), dev(off), E, M_cap, N, K, dB, _ws(moe, n), n)
+    assert moe.moe_get_device_error() == 0
+    got = host_f32_from_bf16(dB)
+    for e in range(E):
+        if counts[e] == 0:
+            assert np.all(host_bf16_bits(dB)[e] == 0)
+        else:
+            assert_close_bf16(got[e], ref[e])
+
+
 def test_invalid_offsets_are_reported_and_nothing_is_read(moe):
     E, M_cap, N, K = 3, 100, 64, 64
     off = np.array([0, 60, 50, 100], np.int32)           # decreasing
