@@ -29,7 +29,9 @@
 // its 128 features exist (I = 2880: 2880 = 22.5 x 128), is an M = 128 pair
 // MMA instead (N rounded up to 32): each CTA stages 64 weight rows (32
 // features) and its accumulator holds weight row l % 64 for tokens
-// (l / 64) * N/2 + column in lane l, columns below N/2.
+// (l / 64) * N/2 + column in lane l, columns below N/2.  So is an expert's
+// last store tile with at most 128 of its 256 features (forward and data
+// gradient; the weight gradient keeps M = 256 there, which measured faster).
 //
 // FP8 (and gathered A): single CTAs, 128 rows (tokens) x 256 columns
 // (weights), 48 KB per k-block, four deep.  Each 128-wide k-block is an exact
@@ -203,9 +205,9 @@ constexpr int kWgA = 0, kWgC = 1, kWgTailA = 2, kWgTailC = 3, kWgMaps = 4;
 struct Tile {
     int e, row0, row_end, col0;
     int rows;  // swapped: token rows of this tile (<= BT)
-    // swapped SwiGLU: the expert's last feature tile, at most half used
-    // (<= 64 h features), runs as an M = 128 pair MMA (each CTA: 32
-    // features' 64 gate and up rows)
+    // swapped forward and data gradient: the expert's last feature tile, at
+    // most half used (<= 64 h features for SwiGLU, <= 128 features for a
+    // store), runs as an M = 128 pair MMA (64 weight rows per CTA)
     bool half;
     int nkb;    // the tile's k-blocks
     int first;  // weight gradient: the expert's first row
@@ -260,7 +262,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& S, const Params
         ti.rows = 0;
     }
     ti.col0 = (local / mt) * (SWAP ? (p.half ? kSwapFeatSwiglu : kSwapFeatStore) : (p.half ? BN / 2 : BN));
-    if (SWAP && !WG && p.half) ti.half = p.half - ti.col0 <= kSwapFeatSwiglu / 2;
+    if (SWAP && p.half && !WG) ti.half = p.half - ti.col0 <= kSwapFeatSwiglu / 2;
+    else if (SWAP && !p.half && !p.fc && !WG) ti.half = p.N - ti.col0 <= kSwapFeatStore / 2;
     return ti;
 }
 
@@ -404,7 +407,7 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW, cons
         const int xrow = ti.row0 + static_cast<int>(rank) * nh;
         // weight gradient: this CTA's nh columns of dC in one or two 64-wide boxes
         const int xbytes = WG ? (nh > 64 ? 2 : 1) * 8192 : nh * 128;
-        const int abytes = ti.half ? kStageA / 2 : kStageA;   // M = 128: 64 weight rows per CTA (SwiGLU)
+        const int abytes = ti.half ? kStageA / 2 : kStageA;   // M = 128: 64 weight rows per CTA
         const int nkb = WG ? ti.nkb : p.k_blocks;
         const int nfull = WG ? (p.offsets[ti.e + 1] - ti.first) / 64 : 0;   // k-blocks read in place
         for (int kb = 0; kb < nkb; ++kb) {
@@ -434,10 +437,12 @@ __device__ void producer_swap(const TokenMaps* tmX, const CUtensorMap* tmW, cons
                     moe::tma_load_2d_pair(sb, mc, fb, xrow, row);
                     if (nh > 64) moe::tma_load_2d_pair(sb + 8192, mc, fb, xrow + 64, row);
                 } else if (EPI == EPI_STORE && p.mn_a) {
-                    // two 64-feature x 64-row swizzle atoms, 8 KB apart
-                    const int f0 = ti.col0 + static_cast<int>(rank) * 128;
+                    // two 64-feature x 64-row swizzle atoms, 8 KB apart (one for M = 128)
+                    const int f0 = ti.col0 + static_cast<int>(rank) * (ti.half ? 64 : 128);
                     moe::tma_load_3d_pair(sa, tmW, fb, f0, kc, ti.e);
-                    moe::tma_load_3d_pair(sa + 8192, tmW, fb, f0 + 64, kc, ti.e);
+                    if (!ti.half) moe::tma_load_3d_pair(sa + 8192, tmW, fb, f0 + 64, kc, ti.e);
+                } else if (EPI == EPI_STORE && ti.half) {   // 64 weight rows
+                    moe::tma_load_3d_pair(sa, tmW64, fb, kc, ti.col0 + static_cast<int>(rank) * 64, ti.e);
                 } else if (EPI == EPI_STORE) {
                     moe::tma_load_3d_pair(sa, tmW, fb, kc, ti.col0 + static_cast<int>(rank) * 128, ti.e);
                 } else if (ti.half) {   // 4 groups: this CTA's 32 features
@@ -578,9 +583,9 @@ __device__ void mma_issuer(uint8_t* stages, Shared& S, const Params& p, int tota
         if (SWAP) {
             const Tile ti = decode_tile<true, WG>(t, S, p);
             const int n = swap_n(ti);
+            const int m = ti.half ? BM : 2 * BM;
             idesc = WG ? moe::make_idesc_ab_mn(1u, 2 * BM, n)
-                 : EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, 2 * BM, n)
-                 : moe::make_idesc(1u, ti.half ? BM : 2 * BM, n);
+                 : EPI == EPI_STORE && p.mn_a ? moe::make_idesc_a_mn(1u, m, n) : moe::make_idesc(1u, m, n);
         }
         if (!FP8) {
             // with a pair, the peer's epilogue arrives here from the other CTA
@@ -779,6 +784,31 @@ __device__ void fused_combine_empty_tokens(const Params& p) {
     }
 }
 
+// Store M = 128 tile (forward and data gradient): lane l of this CTA holds
+// weight row (output feature) l % 64 for token (l / 64) * nh + column, columns
+// below nh = N/2.  Each half of the epilogue takes 64 columns.
+__device__ __forceinline__ void store_half_tile(const Params& p, const Tile& ti, uint32_t ta, int q, int hsel,
+                                                int lane, uint32_t rank) {
+    const int nh = swap_n(ti) / 2, tok0 = (q >> 1) * nh, ntok = ti.rows;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    const int f = ti.col0 + static_cast<int>(rank) * 64 + (q & 1) * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+        const int col = hsel * 64 + c * 32;
+        if (col >= nh || tok0 + col >= ntok) break;   // the same for the whole warp
+        const int jmax = min(32, min(nh - col, ntok - tok0 - col));   // token columns of the chunk
+        uint32_t v[32];
+        moe::tmem_ld32(ta + col, v);
+        moe::tmem_ld_wait();
+        if (f < p.out_cols) {
+            __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + tok0 + col) * p.out_cols + f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < jmax) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+    }
+}
+
 // SwiGLU M = 128 tile: lane l of this CTA holds weight row l % 64 (its 32
 // features' gate and up rows, interleaved in groups of 8 as in a full tile)
 // for token (l / 64) * nh + column, columns below nh = N/2.  Each half of the
@@ -848,6 +878,8 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                                  (WG ? static_cast<int64_t>(ti.e) * p.wg_rows * p.out_cols : 0);
             if (EPI != EPI_STORE && ti.half) {
                 swiglu_half_tile(p, ti, ta, q, hsel, lane, rank);
+            } else if (EPI == EPI_STORE && ti.half) {
+                store_half_tile(p, ti, ta, q, hsel, lane, rank);
             } else {
     #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -1383,13 +1415,16 @@ moe_status_t run_grouped_gemm(moe_dtype_t dtype, const void* A, const float* A_s
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(K) * N * 2};
         const cuuint32_t box[3] = {64, 64, 1};
         if (!encode(&tmB, false, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
-        tmA = tmB;   // unused here; the kernel only prefetches it
+        tmA = tmB;   // the M = 128 tiles load one of these boxes per CTA; tmA is only prefetched
     } else if (!swiglu) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * esz, static_cast<cuuint64_t>(N) * K * esz};
         const cuuint32_t box[3] = {bk, swap ? 128u : BN, 1};   // swapped: 128 weight rows per CTA
         if (!encode(&tmB, fp8, B, 3, dims, strides, box)) return MOE_ERR_CUDA;
-        if (swap) tmA = tmB;   // unused by the swapped store kernel; it only prefetches it
+        // swapped: tmA holds the same weights in boxes of 64 rows, for the
+        // M = 128 tile at the end of an expert's features
+        const cuuint32_t box64[3] = {bk, 64u, 1};
+        if (swap && !encode(&tmA, fp8, B, 3, dims, strides, box64)) return MOE_ERR_CUDA;
     } else if (swap) {
         // [E, N/2/8, 2, 8, K] in memory order (expert, group of 8 features,
         // gate/up, feature in group, k): one box holds 8 groups of 8 gate rows

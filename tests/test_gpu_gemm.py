@@ -200,6 +200,29 @@ def test_bf16_256_experts(moe, epi):
     assert np.all(host_bf16_bits(C)[live:] == 0)
 
 
+# The last store feature tile of an expert holds N mod 256 features; when
+# that is at most 128 it runs as an M = 128 pair MMA.  N = 8 .. 384 puts 8,
+# 64, 128, 8, 64 and 128 features there; N = 392 (136 features) is the
+# M = 256 control.
+@pytest.mark.parametrize("counts", ["boundaries", "box_heights"])
+@pytest.mark.parametrize("N", [8, 64, 128, 264, 320, 384, 392])
+def test_bf16_store_half_used_last_tile(moe, N, counts):
+    counts = PAIR_COUNTS if counts == "boundaries" else BOX_COUNTS
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    live = int(off[-1])
+    M_cap, K = live + 24, 128
+    A = synth.grouped_rows(M_cap, K, live, seed=N + 3)
+    B = _weights(E, N, K, 10)
+    ref = oracle.grouped_gemm_bf16(A, B, off)
+    C = torch.full((M_cap, N), 11, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    moe.moe_grouped_gemm(moe.MOE_BF16, dev_bf16(A), None, dev_bf16(B), None, dev(off), E, M_cap, N, K,
+                         moe.MOE_EPI_STORE, C, None)
+    assert moe.moe_get_device_error() == 0
+    assert_close_bf16(host_f32_from_bf16(C)[:live], ref[:live])
+    assert np.all(host_bf16_bits(C)[live:] == 0)
+
+
 # The last SwiGLU feature tile of an expert holds I mod 128 features; when
 # that is at most 64 it runs as an M = 128 pair MMA (its own accumulator
 # layout, N rounded up to 32).  I = 8 .. 192 puts 8, 40, 64, 8, 56 and 64
