@@ -70,6 +70,25 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def write_peak(torch):
+    """Write-only HBM bandwidth measured here: a 1 GiB fill of a float32 buffer
+    (4-byte stores; torch's fills of 1- and 2-byte elements stop near half of
+    this), timed with CUDA events, median of 10 after 3 warm-up runs."""
+    buf = torch.empty((1 << 30) // 4, dtype=torch.float32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        buf.zero_()
+    ts = []
+    for _ in range(10):
+        e0.record()
+        buf.zero_()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    del buf
+    return (1 << 30) / (statistics.median(ts) * 1e-3) / 1e9
+
+
 def route_kernels(T: int, E: int, k: int) -> int:
     """Kernels moe_route_sort launches: two, or one for a small batch -- a
     single sort block (T*k <= 1024) with at most four (tokens per warp) x
@@ -306,8 +325,11 @@ def flops_bytes(wl, live_rows, experts_live, separate_scatter=False):
     bc = live_rows * H * 2 + R * 12 + T * H * 2
     bq = T * H * 2 + T * H + T * (H // 128) * 4
     br = T * E * 4 + R * 20
+    # the part of each data-movement kernel's bytes that is written
+    wr = dict(permute_bytes=live_rows * (H * ab + sa), combine_bytes=T * H * 2,
+              act_quant_bytes=T * H + T * (H // 128) * 4, route_bytes=R * 20)
     return dict(gemm1_flop=f1, gemm2_flop=f2, gemm1_bytes=b1, gemm2_bytes=b2, permute_bytes=bp,
-                combine_bytes=bc, act_quant_bytes=bq, route_bytes=br)
+                combine_bytes=bc, act_quant_bytes=bq, route_bytes=br, written=wr)
 
 
 def layer_summary(wl, step, step_ms, separate, pk):
@@ -346,10 +368,14 @@ def layer_summary(wl, step, step_ms, separate, pk):
         if name in kt:
             gbs = fb[key] / (kt[name] * 1e-3) / 1e9
             data[name] = {"ms": kt[name], "gbs": gbs, "hbm_frac": gbs / hbm, "algorithmic_bytes": fb[key]}
+            if pk.get("write_gbs"):
+                wgbs = fb["written"][key] / (kt[name] * 1e-3) / 1e9
+                data[name].update({"written_bytes": fb["written"][key], "write_gbs": wgbs,
+                                   "write_frac": wgbs / pk["write_gbs"]})
     ms = statistics.fmean(step_ms)
     return {"ms_per_step": ms, "tokens_per_s": wl.T / (ms * 1e-3), "live_rows": live,
             "experts_with_rows": experts_live, "kernels_ms": kt, "gemm": gemm, "data_movement": data,
-            "peaks": {"tensor_tflops": tpeak, "hbm_gbs": hbm,
+            "peaks": {"tensor_tflops": tpeak, "hbm_gbs": hbm, "write_gbs": pk.get("write_gbs"),
                       "tensor_source": ("fp8 = 2 x " if fp8 else "") + "measured bf16 burst (cuBLAS)"},
             "_fb": fb}
 
@@ -663,9 +689,9 @@ def grad_main(args, wl, synth, torch, moe):
         "down wgrad": lambda: moe.moe_grouped_gemm_wgrad(h, dY2, off, E, R, H, I, dW2, ws, ws_n),
     }
     flop = {"gate_up": 2.0 * live * 2 * I * H, "down": 2.0 * live * H * I}
-    # wgrad writes the whole dB (E * N * K bf16): a second bound besides the
-    # tensor pipe, against the write-only bandwidth measured here as a memset
-    # of the gate_up dB buffer, timed like the ops
+    # wgrad writes the whole dB (E * N * K bf16): its write rate against the
+    # write-only bandwidth measured here as a fill of the gate_up dB buffer
+    # viewed as float32 (4-byte stores), timed like the ops
     out_bytes = {"gate_up": dW1.numel() * 2, "down": dW2.numel() * 2}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -684,7 +710,7 @@ def grad_main(args, wl, synth, torch, moe):
             ts.append(e0.elapsed_time(e1))
         return statistics.fmean(ts)
 
-    write_gbs = out_bytes["gate_up"] / (timed(lambda: dW1.zero_()) * 1e-3) / 1e9
+    write_gbs = out_bytes["gate_up"] / (timed(lambda: dW1.view(torch.float32).zero_()) * 1e-3) / 1e9
     rows = []
     for name, f in ops.items():
         ms = timed(f)
@@ -702,7 +728,8 @@ def grad_main(args, wl, synth, torch, moe):
                                  "activations and output gradients in place and includes the copy of "
                                  "each expert's partial last 64 rows"},
                       "peak": {"bf16_tflops": pk["bf16_tflops"], "kind": pk_kind,
-                               "write_gbs": write_gbs, "write_kind": "memset of the gate_up dB buffer, measured here"},
+                               "write_gbs": write_gbs,
+                               "write_kind": "float32 fill of the gate_up dB buffer, measured here"},
                       "rows": rows}))
     return 0
 
@@ -1014,6 +1041,7 @@ def main():
 
     # ---- roofline of the dominant kernel (the gate_up grouped GEMM)
     pk, pk_kind = peaks()
+    pk = dict(pk, write_gbs=write_peak(torch))
     summ = layer_summary(wl, step, step_ms, separate, pk)
     fb = summ.pop("_fb")
     live, experts_live = summ["live_rows"], summ["experts_with_rows"]
@@ -1080,7 +1108,9 @@ def main():
         "kernels_ms": summ["kernels_ms"],
         "hbm": {"permute_gbs": summ["data_movement"].get("permute", {}).get("gbs"),
                 "combine_gbs": summ["data_movement"].get("combine", {}).get("gbs"),
-                "peak_gbs": pk["hbm_gbs"], "detail": summ["data_movement"]},
+                "peak_gbs": pk["hbm_gbs"], "write_peak_gbs": pk["write_gbs"],
+                "write_peak_source": "1 GiB float32 fill timed in this run (write-only HBM bandwidth)",
+                "detail": summ["data_movement"]},
         "e2e": {"value": job_tokens_per_s(wl.T, world, e2e_capi_max), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2,
