@@ -881,7 +881,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
             } else if (EPI == EPI_STORE && ti.half) {
                 store_half_tile(p, ti, ta, q, hsel, lane, rank);
             } else {
-    #pragma unroll 1
+#pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     const int col = hsel * 128 + c * 32;
                     if (col >= ntok) break;                       // the same for the whole warp
@@ -890,7 +890,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                         moe::tmem_ld32(ta + col, v);
                         moe::tmem_ld_wait();
                     } else {   // an expert without rows: its weight gradient is zero
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0u;
                     }
                     if (EPI == EPI_STORE) {
@@ -899,7 +899,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                         const int f = ti.col0 + static_cast<int>(rank) * 128 + q * 32 + lane;
                         if (f < p.out_cols) {
                             __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + col) * p.out_cols + f;
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 32; ++j)
                                 if (col + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(__uint_as_float(v[j]));
                         }
@@ -911,7 +911,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                         // other's values for its tokens.
                         const int r = (lane >> 3) & 1;            // 0: gate lane, 1: up lane
                         float h[16];
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[16 + j]);
                             const float o = __shfl_xor_sync(0xffffffffu, r ? lo : hi, 8);
@@ -921,7 +921,7 @@ __device__ void epilogue(Shared& S, const Params& p, int total, uint32_t tmem, u
                         const int t0 = col + 16 * r;
                         if (f < p.out_cols) {
                             __nv_bfloat16* o = out + static_cast<int64_t>(ti.row0 + t0) * p.out_cols + f;
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 if (t0 + j < ntok) o[static_cast<int64_t>(j) * p.out_cols] = __float2bfloat16_rn(h[j]);
                         }
