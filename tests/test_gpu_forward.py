@@ -68,6 +68,9 @@ LAYERS = [
     synth.WORKLOADS["tiny-8e-top2"],
     synth.Workload("mid-16e-top4", T=300, E=16, k=4, H=256, I=384, n_sentinel=40, bias="normal0.5"),
     synth.Workload("ragged-12e-top3", T=97, E=12, k=3, H=136, I=200, n_sentinel=5),
+    # a larger batch: several token tiles per expert, ragged rows (17
+    # vectors), 400 sentinel slots
+    synth.Workload("large-16e-top4", T=3000, E=16, k=4, H=136, I=200, n_sentinel=400, bias="normal0.5"),
 ]
 
 
